@@ -1,0 +1,139 @@
+/*
+ * pfa.h -- C ABI of libpfa: stabilised BF16 flash attention (forward and
+ * backward) for one GB300 GPU (sm_103a).
+ *
+ * The method is the one analysed in Qiu & Yao, "Why Low-Precision Transformer
+ * Training Fails: An Analysis on Flash Attention" (ICLR 2026). Citations name the
+ * page that describes each operation:
+ *   [PK] priors.kr post "BF16 플래시 어텐션은 왜 수천 스텝 뒤에 무너질까"
+ *   [BN] bud-325 note "Why Low-Precision Transformer Training Fails: An Analysis
+ *        on Flash Attention"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are dense, contiguous, row-major [B, H, N, d] with d innermost
+ *    ("BHND"). Q, O, dO, dQ have H = H_q heads; K, V, dK, dV have H = H_kv heads;
+ *    query head h reads key/value head h / (H_q / H_kv). lse and delta are
+ *    [B, H_q, N] FP32.
+ *  - BF16 tensors are passed as pointers to raw bfloat16 bit patterns
+ *    (pfa_bf16). FP32 tensors are float pointers.
+ *  - Every data pointer is DEVICE memory on the current CUDA device, owned by the
+ *    caller, 16-byte aligned. The library allocates nothing and never
+ *    synchronises: all work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and results are ready when that stream reaches them.
+ *  - Supported sizes: B, H_q, H_kv >= 1 with H_q % H_kv == 0; N >= 1 (any length,
+ *    ragged tails are masked); d in {64, 128}; B * H * N * d < 2^31 elements per
+ *    tensor. `scale` is alpha in S = alpha Q K^T and must be finite and > 0
+ *    (1/sqrt(d) is the usual choice). causal != 0 lets query i see keys j <= i.
+ *  - Return value: PFA_OK (0) or a negative PFA_ERR_* code. Arguments are checked
+ *    before anything is enqueued; on an argument error nothing is launched. No
+ *    C++ exception crosses this interface.
+ *  - Kernels never trap. A kernel whose internal pipeline wait exceeds about one
+ *    second gives up, sets a bit in the library's device error word and returns;
+ *    pfa_device_error() reads that word.
+ */
+#ifndef PFA_H_
+#define PFA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pfa_stream_t; /* == cudaStream_t */
+typedef uint16_t pfa_bf16;                /* raw bfloat16 bit pattern */
+
+enum {
+  PFA_OK = 0,
+  PFA_ERR_INVALID_ARG = -1, /* null pointer, bad size, bad mode/beta/eps/scale */
+  PFA_ERR_MISALIGNED = -2,  /* a pointer is not 16-byte aligned */
+  PFA_ERR_UNSUPPORTED = -3, /* no sm_103 device current, or driver lacks TMA map encoding */
+  PFA_ERR_LAUNCH = -4,      /* a CUDA launch or runtime call failed */
+  PFA_ERR_DEVICE = -5       /* pfa_device_error(): a kernel reported a failure */
+};
+
+/* Device error word bits, as returned by pfa_device_error(). */
+#define PFA_DEVERR_TIMEOUT 1    /* a bounded pipeline wait gave up */
+#define PFA_DEVERR_SMEM_ALIGN 2 /* dynamic shared memory was not 1024-byte aligned */
+
+/* Diagnostic counters, int64 each, in DEVICE memory owned by the caller. Calls
+ * ADD to them (the caller zeroes them). Definitions, per row of the forward pass:
+ *   repeated_rows  rows whose maximum score r_m is reached again within eps
+ *                  ([PK] the fix, paper §4; the quantity of paper Fig. 13);
+ *   ones           entries whose BF16 Pbar = exp(S - m) equals 1.0 under the
+ *                  row's final shift m ([PK] core idea: the exact-1 entries that
+ *                  bias the BF16 sum);
+ *   nonfinite_rows rows whose normaliser l is 0 or not finite (the underflow of
+ *                  [PK] caveats / paper App. C). */
+typedef struct pfa_counters {
+  int64_t repeated_rows;
+  int64_t ones;
+  int64_t nonfinite_rows;
+} pfa_counters;
+
+/* Forward pass ([PK] equations and the fix of paper §4; [BN] Method, Algorithm 1).
+ * Per row i: S = alpha q_i K^T over the visible keys, r_m = max S, the row is
+ * "repeated" when a second score lies within `eps` of r_m, and the shift m is
+ *   fix_mode 0: m = r_m (plain safe softmax);
+ *   fix_mode 1: repeated rows m = beta*r_m if r_m > 0, 0 if r_m < 0, 2^-5 if
+ *               r_m == 0; other rows m = r_m;
+ *   fix_mode 2: repeated rows m = r_m + 2^-5; other rows m = r_m.
+ * Pbar = exp(S - m) rounded to BF16, l = sum of those BF16 values,
+ * O = (Pbar V) / l rounded to BF16, lse = m + ln(l) in FP32.
+ *   q [B,H_q,N,d], k, v [B,H_kv,N,d] (in); o [B,H_q,N,d], lse [B,H_q,N] (out).
+ *   beta > 1 (mode 1; [PK] recommends 2..8; ignored otherwise).
+ *   eps >= 0 finite: the tie tolerance ([PK] suggests 1e-3). It selects the rows
+ *   the fix shifts in modes 1 and 2, and the rows counted in repeated_rows (every
+ *   mode); it is ignored in mode 0 without counters.
+ *   counters: optional (NULL skips the counting work).
+ * With the beta shift, rows with a large repeated maximum can underflow (l = 0):
+ * O is then NaN, lse is -inf and the row is counted in nonfinite_rows, as the
+ * pages describe the failure; no guard is applied. */
+int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
+                 int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
+                 float beta, float eps, pfa_counters* counters, pfa_stream_t stream);
+
+/* delta = rowsum(dO o O) in FP32 from the BF16 forward output ([PK] three-line
+ * summary and method, paper §3.2; [BN] Key claims).
+ *   o, dO [B,H_q,N,d] (in); delta [B,H_q,N] (out). */
+int pfa_attn_delta(const pfa_bf16* o, const pfa_bf16* dO, float* delta, int B, int H_q, int N,
+                   int d, pfa_stream_t stream);
+
+/* delta = rowsum(dP o P) with P = exp(alpha Q K^T - lse) and dP = dO V^T
+ * recomputed: the mathematically equal alternative of [PK] method, paper §3.2.
+ *   q, dO [B,H_q,N,d], k, v [B,H_kv,N,d], lse [B,H_q,N] (in); delta (out). */
+int pfa_attn_delta_alt(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                       const float* lse, float* delta, int B, int H_q, int H_kv, int N, int d,
+                       int causal, float scale, pfa_stream_t stream);
+
+/* Backward pass ([PK] equations: dS = alpha P o (dP - delta), dQ = dS K; with
+ * dK = dS^T Q and dV = P^T dO summed over the query heads of a key/value head).
+ * P is recomputed from lse; the fix does not change the backward pass ([PK] the
+ * fix paragraph; [BN] Results).
+ *   q, dO [B,H_q,N,d], k, v [B,H_kv,N,d], lse, delta [B,H_q,N] (in);
+ *   dq [B,H_q,N,d], dk, dv [B,H_kv,N,d] (out, BF16);
+ *   dq_accum: FP32 workspace of pfa_bwd_workspace_bytes() bytes, caller-owned
+ *   device memory; its contents on entry are ignored (it is zeroed on `stream`). */
+int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                 pfa_stream_t stream);
+
+/* Bytes of the dq_accum workspace pfa_attn_bwd needs: B*H_q*N*d*4 (0 on bad sizes). */
+size_t pfa_bwd_workspace_bytes(int B, int H_q, int N, int d);
+
+/* Human-readable name of a PFA_* status code (static string, never NULL). */
+const char* pfa_status_string(int status);
+
+/* Reads (and, if clear != 0, resets) the device error word of the current device.
+ * Returns the PFA_DEVERR_* bits (>= 0) or a negative PFA_ERR_* code. This call
+ * synchronises the current device. */
+int pfa_device_error(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PFA_H_ */

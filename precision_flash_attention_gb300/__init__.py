@@ -1,0 +1,80 @@
+"""Stabilised BF16 flash attention (forward and backward) for one GB300 GPU.
+
+The compute path is libpfa (hand-written sm_103a kernels behind the C ABI in
+``include/pfa.h``); this package is its thin Python binding plus convenience
+wrappers that allocate outputs with torch. There is no CPU or PyTorch fallback:
+calls fail if libpfa has not been built or no sm_103 device is current.
+
+The method is from Qiu & Yao, "Why Low-Precision Transformer Training Fails: An
+Analysis on Flash Attention" (ICLR 2026): rows whose maximum score repeats get a
+different softmax shift so that no BF16 exp(S - m) rounds to exactly 1.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from ._lib import (EXPORTS, PfaError, attn_bwd, attn_delta, attn_delta_alt, attn_fwd,
+                   bwd_workspace_bytes, device_error, load, status_string)
+
+__all__ = [
+    "EXPORTS", "PfaError", "attn_fwd", "attn_delta", "attn_delta_alt", "attn_bwd",
+    "bwd_workspace_bytes", "device_error", "load", "status_string", "forward", "backward",
+    "StabilizedAttention", "new_counters",
+]
+
+
+def new_counters(device="cuda") -> torch.Tensor:
+    """A zeroed int64[3] device buffer for (repeated_rows, ones, nonfinite_rows)."""
+    return torch.zeros(3, dtype=torch.int64, device=device)
+
+
+def forward(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3, counters=None,
+            stream=None):
+    """Allocate O and lse and run pfa_attn_fwd. Returns (o, lse)."""
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps,
+             counters=counters, stream=stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, *, causal=False, scale=None, delta_mode=0, stream=None,
+             workspace=None):
+    """delta (rowsum(dO o O), or rowsum(dP o P) with ``delta_mode=1``) then pfa_attn_bwd.
+
+    Returns (dq, dk, dv, delta)."""
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
+    delta = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if delta_mode == 0:
+        attn_delta(o, do, delta, stream=stream)
+    else:
+        attn_delta_alt(q, k, v, do, lse, delta, causal=causal, scale=scale, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    B, H, N, d = q.shape
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
+                                device=q.device)
+    attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, workspace, causal=causal, scale=scale,
+             stream=stream)
+    return dq, dk, dv, delta
+
+
+class StabilizedAttention(torch.autograd.Function):
+    """Autograd wrapper: ``StabilizedAttention.apply(q, k, v, causal, scale, fix_mode, beta, eps)``."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3):
+        o, lse = forward(q, k, v, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale = causal, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv, _ = backward(q, k, v, o, lse, do.contiguous(), causal=ctx.causal,
+                                 scale=ctx.scale)
+        return dq, dk, dv, None, None, None, None, None

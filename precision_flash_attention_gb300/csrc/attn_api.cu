@@ -1,0 +1,248 @@
+// C ABI of libpfa (declared in include/pfa.h): argument checks, TMA tensor-map
+// encoding, the device error word, and the launch sequence of each entry point.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "pfa_internal.h"
+
+namespace {
+
+// Device error word: kernels OR PFA_DEVERR_* bits into it instead of trapping.
+__device__ int g_pfa_device_error;
+
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+// BF16(exp(x)) == 1.0 exactly when x >= -ln(1 - 2^-9): the round-to-one window.
+constexpr double kRoundToOneWindow = 1.9550348e-3;
+
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int* err = nullptr;  // device address of g_pfa_device_error on this device
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+// Looks up (once per device, with that device current) whether it is an sm_103
+// part and where the error word lives.
+int current_device(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PFA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return PFA_ERR_LAUNCH;
+    st.supported = (major == 10 && minor == 3);
+    if (st.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_pfa_device_error) != cudaSuccess) return PFA_ERR_LAUNCH;
+      st.err = static_cast<int*>(p);
+    }
+    if (!g_encode_tried) {
+      g_encode_tried = true;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  if (!st.supported || g_encode == nullptr) return PFA_ERR_UNSUPPORTED;
+  *out = &st;
+  return PFA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int Hq, int Hkv, int N, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return PFA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return PFA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return PFA_ERR_INVALID_ARG;
+  const long long elems = static_cast<long long>(B) * Hq * N * d;
+  if (elems >= (1ll << 31)) return PFA_ERR_INVALID_ARG;
+  return PFA_OK;
+}
+
+bool good_scale(float s) { return std::isfinite(s) && s > 0.f; }
+
+// [B*H, N, d] BF16 tensor, boxes of 64 columns (128 bytes, 128B swizzle) x 128 rows.
+int tile_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pfa::kTile), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PFA_OK : PFA_ERR_INVALID_ARG;
+}
+
+pfa::AttnShape shape(int B, int Hq, int Hkv, int N, int d, int causal, float scale) {
+  pfa::AttnShape s;
+  s.B = B;
+  s.Hq = Hq;
+  s.Hkv = Hkv;
+  s.N = N;
+  s.d = d;
+  s.causal = causal ? 1 : 0;
+  s.scale = scale;
+  s.scale_log2 = scale * kLog2e;
+  return s;
+}
+
+int launched(cudaError_t e) { return e == cudaSuccess ? PFA_OK : PFA_ERR_LAUNCH; }
+
+}  // namespace
+
+extern "C" {
+
+int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
+                 int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
+                 float beta, float eps, pfa_counters* counters, pfa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return PFA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H_q, H_kv, N, d);
+  if (rc != PFA_OK) return rc;
+  if (!good_scale(scale) || fix_mode < 0 || fix_mode > 2) return PFA_ERR_INVALID_ARG;
+  if (fix_mode == 1 && !(std::isfinite(beta) && beta > 1.f)) return PFA_ERR_INVALID_ARG;
+  const bool ties = fix_mode != 0 || counters != nullptr;
+  if (ties && !(std::isfinite(eps) && eps >= 0.f)) return PFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (counters && (reinterpret_cast<uintptr_t>(counters) & 7u)))
+    return PFA_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != PFA_OK) return rc;
+  CUtensorMap tq, tk, tv;
+  if ((rc = tile_map(&tq, q, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
+  pfa::FwdArgs a;
+  a.s = shape(B, H_q, H_kv, N, d, causal, scale);
+  a.o = o;
+  a.lse = lse;
+  a.counters = reinterpret_cast<long long*>(counters);
+  a.err = dev->err;
+  a.fix_mode = fix_mode;
+  a.beta = fix_mode == 1 ? beta : 2.f;
+  a.eps_raw = ties ? eps / scale : 0.f;
+  a.tau_raw = static_cast<float>(kRoundToOneWindow / scale);
+  return launched(pfa::launch_fwd(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pfa_attn_delta(const pfa_bf16* o, const pfa_bf16* dO, float* delta, int B, int H_q, int N,
+                   int d, pfa_stream_t stream) {
+  if (!o || !dO || !delta) return PFA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H_q, H_q, N, d);
+  if (rc != PFA_OK) return rc;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta)) return PFA_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != PFA_OK) return rc;
+  return launched(pfa::launch_delta(o, dO, delta, static_cast<long long>(B) * H_q * N, d,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int pfa_attn_delta_alt(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                       const float* lse, float* delta, int B, int H_q, int H_kv, int N, int d,
+                       int causal, float scale, pfa_stream_t stream) {
+  if (!q || !k || !v || !dO || !lse || !delta) return PFA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H_q, H_kv, N, d);
+  if (rc != PFA_OK) return rc;
+  if (!good_scale(scale)) return PFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(delta))
+    return PFA_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != PFA_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = tile_map(&tq, q, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
+  pfa::DeltaAltArgs a;
+  a.s = shape(B, H_q, H_kv, N, d, causal, scale);
+  a.lse = lse;
+  a.delta = delta;
+  a.err = dev->err;
+  return launched(pfa::launch_delta_alt(tq, tk, tv, tdo, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pfa_bwd_workspace_bytes(int B, int H_q, int N, int d) {
+  if (check_sizes(B, H_q, H_q, N, d) != PFA_OK) return 0;
+  return static_cast<size_t>(B) * H_q * N * d * sizeof(float);
+}
+
+int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                 pfa_stream_t stream) {
+  if (!q || !k || !v || !dO || !lse || !delta || !dq || !dk || !dv || !dq_accum)
+    return PFA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H_q, H_kv, N, d);
+  if (rc != PFA_OK) return rc;
+  if (!good_scale(scale)) return PFA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
+      !aligned16(delta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      !aligned16(dq_accum))
+    return PFA_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != PFA_OK) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((rc = tile_map(&tq, q, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
+  if (cudaMemsetAsync(dq_accum, 0, ws, st) != cudaSuccess) return PFA_ERR_LAUNCH;
+  pfa::BwdArgs a;
+  a.s = shape(B, H_q, H_kv, N, d, causal, scale);
+  a.lse = lse;
+  a.delta = delta;
+  a.dq_accum = dq_accum;
+  a.dk = dk;
+  a.dv = dv;
+  a.err = dev->err;
+  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, a, st))) != PFA_OK) return rc;
+  return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
+}
+
+const char* pfa_status_string(int status) {
+  switch (status) {
+    case PFA_OK: return "PFA_OK";
+    case PFA_ERR_INVALID_ARG: return "PFA_ERR_INVALID_ARG: invalid pointer, size, mode, beta, eps or scale";
+    case PFA_ERR_MISALIGNED: return "PFA_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case PFA_ERR_UNSUPPORTED: return "PFA_ERR_UNSUPPORTED: current device is not sm_103 or TMA encoding is unavailable";
+    case PFA_ERR_LAUNCH: return "PFA_ERR_LAUNCH: a CUDA launch or runtime call failed";
+    case PFA_ERR_DEVICE: return "PFA_ERR_DEVICE: a kernel reported a failure in the device error word";
+    default: return "PFA_ERR_UNKNOWN";
+  }
+}
+
+int pfa_device_error(int clear) {
+  DeviceState* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != PFA_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PFA_ERR_LAUNCH;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_pfa_device_error, sizeof(int)) != cudaSuccess) return PFA_ERR_LAUNCH;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_pfa_device_error, &zero, sizeof(int)) != cudaSuccess) return PFA_ERR_LAUNCH;
+  }
+  return word;
+}
+
+}  // extern "C"

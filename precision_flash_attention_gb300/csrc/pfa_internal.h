@@ -1,0 +1,61 @@
+// Internal declarations shared by the host-side launchers of libpfa.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pfa.h"  // status codes and the PFA_DEVERR_* bits kernels OR into the error word
+
+namespace pfa {
+
+constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
+
+// Arguments common to the tiled kernels (all sizes in elements).
+struct AttnShape {
+  int B, Hq, Hkv, N, d;
+  int causal;
+  float scale;        // alpha
+  float scale_log2;   // alpha * log2(e)
+};
+
+struct FwdArgs {
+  AttnShape s;
+  void* o;                 // bf16 [B, Hq, N, d]
+  float* lse;              // [B, Hq, N]
+  long long* counters;     // 3 x int64 or null
+  int* err;                // device error word
+  int fix_mode;
+  float beta;
+  float eps_raw;           // tie tolerance in units of the unscaled score Q.K
+  float tau_raw;           // BF16 round-to-one window in units of Q.K
+};
+
+struct DeltaAltArgs {
+  AttnShape s;
+  const float* lse;
+  float* delta;
+  int* err;
+};
+
+struct BwdArgs {
+  AttnShape s;
+  const float* lse;
+  const float* delta;
+  float* dq_accum;         // fp32 [B, Hq, N, d], zeroed before the launch
+  void* dk;                // bf16 [B, Hkv, N, d]
+  void* dv;                // bf16 [B, Hkv, N, d]
+  int* err;
+};
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long rows, int d,
+                         cudaStream_t stream);
+cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const CUtensorMap& tdo, const DeltaAltArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream);
+
+}  // namespace pfa

@@ -1,0 +1,91 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI, run the
+oracle on the same seeded inputs, and compare with the float tolerances of the contract:
+O and lse rel-L2 <= 4e-3 and max-abs <= 1.5e-2; dQ, dK, dV (and delta) rel-L2 <= 1e-2."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import precision_flash_attention_gb300 as pfa
+
+TOL_FWD_REL = 4e-3
+TOL_FWD_ABS = 1.5e-2
+TOL_BWD_REL = 1e-2
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    nb = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (nb if nb > 0 else 1.0))
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def to_dev(t: dict) -> dict:
+    return {n: x.cuda() for n, x in t.items()}
+
+
+def run_gpu(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True, delta_mode=0):
+    """Forward (+ delta + backward) on the GPU; returns numpy float64 results and counters."""
+    d = to_dev(t)
+    cnt = pfa.new_counters()
+    o, lse = pfa.forward(d["q"], d["k"], d["v"], causal=causal, scale=scale, fix_mode=fix_mode,
+                         beta=beta, eps=eps, counters=cnt)
+    out = {"o": o, "lse": lse}
+    if bwd:
+        dq, dk, dv, delta = pfa.backward(d["q"], d["k"], d["v"], o, lse, d["do"], causal=causal,
+                                         scale=scale, delta_mode=delta_mode)
+        out.update(dq=dq, dk=dk, dv=dv, delta=delta)
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    res = {n: f64(x) for n, x in out.items()}
+    c = cnt.cpu().tolist()
+    res["counters"] = {"repeated_rows": c[0], "ones": c[1], "nonfinite_rows": c[2]}
+    return res
+
+
+def oracle_full(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True):
+    q, k, v, do = (f64(t[n]) for n in ("q", "k", "v", "do"))
+    f = oracle.attn_fwd(q, k, v, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps)
+    out = {"o": f["o"], "lse": f["lse"], "counters": f["counters"]}
+    if bwd:
+        delta = oracle.attn_delta(f["o"], do)
+        g = oracle.attn_bwd(q, k, v, do, f["lse"], delta, causal=causal, scale=scale)
+        out.update(g, delta=delta)
+    return out
+
+
+def assert_fwd_close(got: dict, ref: dict, where: str = "") -> None:
+    for n in ("o", "lse"):
+        a, b = got[n], ref[n]
+        assert np.isfinite(a).all(), f"{where} {n} has non-finite values"
+        r = rel_l2(a, b)
+        m = float(np.abs(a - b).max())
+        assert r <= TOL_FWD_REL and m <= TOL_FWD_ABS, f"{where} {n}: rel-L2 {r:.3e}, max-abs {m:.3e}"
+
+
+def assert_bwd_close(got: dict, ref: dict, where: str = "", names=("dq", "dk", "dv")) -> None:
+    for n in names:
+        a, b = got[n], ref[n]
+        assert np.isfinite(a).all(), f"{where} {n} has non-finite values"
+        r = rel_l2(a, b)
+        assert r <= TOL_BWD_REL, f"{where} {n}: rel-L2 {r:.3e}"
+
+
+def oracle_group(t: dict, b: int, hk: int, *, causal, scale, fix_mode, beta=2.0, eps=1e-3):
+    """Oracle forward + backward restricted to batch b and key/value head hk with all the
+    query heads that read it (dK and dV sum over exactly those heads)."""
+    Hq, Hkv = t["q"].shape[1], t["k"].shape[1]
+    g = Hq // Hkv
+    hs = slice(hk * g, (hk + 1) * g)
+    q = f64(t["q"][b:b + 1, hs])
+    do = f64(t["do"][b:b + 1, hs])
+    k = f64(t["k"][b:b + 1, hk:hk + 1])
+    v = f64(t["v"][b:b + 1, hk:hk + 1])
+    f = oracle.attn_fwd(q, k, v, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps)
+    delta = oracle.attn_delta(f["o"], do)
+    gr = oracle.attn_bwd(q, k, v, do, f["lse"], delta, causal=causal, scale=scale)
+    return {"o": f["o"][0], "lse": f["lse"][0], "delta": delta[0], "dq": gr["dq"][0],
+            "dk": gr["dk"][0, 0], "dv": gr["dv"][0, 0], "counters": f["counters"], "heads": hs}

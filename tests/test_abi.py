@@ -1,0 +1,107 @@
+"""The C ABI without a GPU: libpfa builds, loads, exports every declared symbol, and rejects
+bad arguments before it touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from precision_flash_attention_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pfa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return _lib.load()
+
+
+def _declared():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pfa_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(_lib.EXPORTS) == _declared()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.pfa_status_string(code).decode().startswith(name)
+    assert lib.pfa_status_string(12345).decode() == "PFA_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert lib.pfa_bwd_workspace_bytes(8, 12, 1024, 64) == 8 * 12 * 1024 * 64 * 4
+    assert lib.pfa_bwd_workspace_bytes(1, 1, 1, 128) == 512
+    assert lib.pfa_bwd_workspace_bytes(1, 1, 1, 96) == 0
+    assert lib.pfa_bwd_workspace_bytes(0, 1, 16, 64) == 0
+    assert lib.pfa_bwd_workspace_bytes(4096, 64, 8192, 128) == 0  # over 2^31 elements
+
+
+A = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced on these paths
+
+
+def _fwd(lib, **kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=1, N=64, d=64, causal=0, scale=0.125,
+                mode=1, beta=2.0, eps=1e-3, counters=None, stream=None)
+    args.update(kw)
+    return lib.pfa_attn_fwd(*args.values())
+
+
+def test_fwd_argument_errors(lib):
+    inv, mis = -1, -2
+    assert _fwd(lib, q=None) == inv
+    assert _fwd(lib, lse=None) == inv
+    assert _fwd(lib, N=0) == inv
+    assert _fwd(lib, d=96) == inv
+    assert _fwd(lib, Hq=3, Hkv=2) == inv
+    assert _fwd(lib, mode=3) == inv
+    assert _fwd(lib, mode=-1) == inv
+    assert _fwd(lib, beta=1.0) == inv            # the fix needs beta > 1
+    assert _fwd(lib, beta=float("nan")) == inv
+    assert _fwd(lib, eps=-1e-3) == inv
+    assert _fwd(lib, eps=float("inf")) == inv
+    assert _fwd(lib, scale=0.0) == inv
+    assert _fwd(lib, scale=float("nan")) == inv
+    assert _fwd(lib, q=A + 8) == mis
+    assert _fwd(lib, counters=A + 4) == mis
+    # beta is not checked in mode 0/2, eps not in mode 0 without counters: the call gets
+    # past validation and fails only on the missing device.
+    assert _fwd(lib, mode=0, beta=0.5, eps=-1.0) not in (inv, mis)
+    assert _fwd(lib, mode=0, eps=-1.0, counters=A) == inv
+
+
+def test_other_entry_points_validate(lib):
+    inv, mis = -1, -2
+    assert lib.pfa_attn_delta(None, A, A, 1, 1, 64, 64, None) == inv
+    assert lib.pfa_attn_delta(A, A, A + 4, 1, 1, 64, 64, None) == mis
+    assert lib.pfa_attn_delta(A, A, A, 1, 1, 64, 32, None) == inv
+    assert lib.pfa_attn_delta_alt(A, A, A, A, A, A, 1, 2, 1, 64, 64, 1, -1.0, None) == inv
+    assert lib.pfa_attn_delta_alt(A, A, A, A, A, None, 1, 2, 1, 64, 64, 1, 0.1, None) == inv
+    args = [A] * 10 + [1, 2, 1, 64, 64, 1, 0.125, None]
+    bad = list(args)
+    bad[9] = None  # no workspace
+    assert lib.pfa_attn_bwd(*bad) == inv
+    bad = list(args)
+    bad[6] = A + 2
+    assert lib.pfa_attn_bwd(*bad) == mis
+    bad = list(args)
+    bad[12] = 3  # H_kv does not divide H_q
+    assert lib.pfa_attn_bwd(*bad) == inv
+
+
+def test_without_a_device_calls_fail_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert _fwd(lib) in (-3, -4)
+    assert lib.pfa_device_error(0) in (-3, -4)

@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded
+inputs. Float outputs within the contract tolerances; integer counters bit-exact on
+integer-valued inputs, where every score is exact in FP32 and FP64."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_flash_attention_gb300 as pfa
+from precision_flash_attention_gb300 import inputs
+from tests.gpu_helpers import (TOL_BWD_REL, assert_bwd_close, assert_fwd_close, f64, oracle_full,
+                               oracle_group, rel_l2, run_gpu, to_dev)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    pfa.device_error(clear=True)
+
+
+# ---------------------------------------------------------------- tiny workload
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("delta_mode", [0, 1])
+def test_tiny_forward_backward(mode, delta_mode):
+    t = inputs.make("tiny", seed=0)
+    got = run_gpu(t, causal=False, scale=0.125, fix_mode=mode, delta_mode=delta_mode)
+    ref = oracle_full(t, causal=False, scale=0.125, fix_mode=mode)
+    assert_fwd_close(got, ref, f"tiny mode {mode}")
+    assert_bwd_close(got, ref, f"tiny mode {mode} delta_mode {delta_mode}")
+    assert rel_l2(got["delta"], ref["delta"]) <= TOL_BWD_REL
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 64, 64), (2, 4, 2, 200, 64), (1, 2, 1, 384, 128),
+                                   (1, 3, 3, 129, 128)])
+def test_grid_counters_bit_exact(mode, causal, shape):
+    # Integer Q, K in [-4, 4] with planted duplicated maxima: scores are exact multiples of 1/8.
+    B, Hq, Hkv, N, d = shape
+    t = inputs.integer_grid(B, Hq, Hkv, N, d, causal=causal, n_planted=8, seed=N + d + mode)
+    got = run_gpu(t, causal=causal, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
+    ref = oracle_full(t, causal=causal, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
+    assert ref["counters"]["repeated_rows"] >= 8
+    assert got["counters"] == ref["counters"]
+    assert_fwd_close(got, ref, "grid")
+    assert_bwd_close(got, ref, "grid")
+
+
+# ---------------------------------------------------------------- ragged shapes
+RAGGED = [
+    # B, Hq, Hkv, N, d, causal
+    (1, 1, 1, 1, 64, True),
+    (1, 2, 1, 7, 64, False),
+    (2, 2, 2, 65, 64, True),
+    (1, 4, 2, 100, 128, True),
+    (1, 1, 1, 129, 64, False),
+    (1, 2, 2, 257, 128, False),
+    (2, 3, 1, 300, 64, True),
+    (1, 2, 1, 640, 128, True),
+]
+
+
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_ragged_shapes(shape, mode):
+    B, Hq, Hkv, N, d, causal = shape
+    t = inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.7, std_do=1.0, seed=7 * N + d)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(t, causal=causal, scale=scale, fix_mode=mode, beta=3.0)
+    ref = oracle_full(t, causal=causal, scale=scale, fix_mode=mode, beta=3.0)
+    assert_fwd_close(got, ref, f"{shape} mode {mode}")
+    assert_bwd_close(got, ref, f"{shape} mode {mode}")
+    assert got["counters"]["nonfinite_rows"] == 0
+
+
+def test_delta_alt_equals_delta():
+    # rowsum(dP o P) and rowsum(dO o O) agree (the identity of the paper's §3.2).
+    t = inputs.gaussian(2, 4, 2, 333, 64, std_qkv=0.5, std_do=1.0, seed=3)
+    d = to_dev(t)
+    o, lse = pfa.forward(d["q"], d["k"], d["v"], causal=True, scale=0.125)
+    d0 = torch.empty_like(lse)
+    d1 = torch.empty_like(lse)
+    pfa.attn_delta(o, d["do"], d0)
+    pfa.attn_delta_alt(d["q"], d["k"], d["v"], d["do"], lse, d1, causal=True, scale=0.125)
+    torch.cuda.synchronize()
+    ref = oracle_full(t, causal=True, scale=0.125, fix_mode=0)["delta"]
+    assert rel_l2(f64(d0), ref) <= TOL_BWD_REL
+    assert rel_l2(f64(d1), ref) <= TOL_BWD_REL
+    # delta from the GPU's own O is FP32 arithmetic on BF16 data: near-exact.
+    exact = oracle.attn_delta(f64(o), f64(t["do"]))
+    np.testing.assert_allclose(f64(d0), exact, rtol=1e-5, atol=1e-5)
+
+
+# ---------------------------------------------------------------- full-size workloads
+def test_gpt2_small_layer_all_heads():
+    # B=8, H=12, N=1024, d=64, causal, modes 0 and 1 (beta=2): every head against the oracle.
+    t = inputs.make("gpt2", seed=0)
+    for mode in (0, 1):
+        got = run_gpu(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0)
+        ref = oracle_full(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0)
+        assert_fwd_close(got, ref, f"gpt2 mode {mode}")
+        assert_bwd_close(got, ref, f"gpt2 mode {mode}")
+        assert got["counters"]["nonfinite_rows"] == 0
+        # ones >= rows in mode 0: every row's maximum gives Pbar = 1 exactly.
+        rows = 8 * 12 * 1024
+        if mode == 0:
+            assert got["counters"]["ones"] >= rows
+        # the repeated-row count is the same tie detector in every mode (fp32 vs fp64 scores
+        # may move a handful of borderline rows)
+        assert abs(got["counters"]["repeated_rows"] - ref["counters"]["repeated_rows"]) <= 8
+
+
+def _check_groups(t, got, groups, *, causal, scale, mode, beta):
+    for b, hk in groups:
+        r = oracle_group(t, b, hk, causal=causal, scale=scale, fix_mode=mode, beta=beta)
+        hs = r["heads"]
+        assert_fwd_close({"o": got["o"][b, hs], "lse": got["lse"][b, hs]}, r, f"group {b},{hk}")
+        assert_bwd_close({"dq": got["dq"][b, hs], "dk": got["dk"][b, hk], "dv": got["dv"][b, hk]},
+                         r, f"group {b},{hk}")
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_sink_heavy(mode):
+    t = inputs.make("sink", seed=0)
+    got = run_gpu(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0)
+    _check_groups(t, got, [(0, 0), (3, 11), (1, 5)], causal=True, scale=0.125, mode=mode, beta=2.0)
+    c = got["counters"]
+    assert c["nonfinite_rows"] == 0
+    assert c["repeated_rows"] > 0.1 * 4 * 12 * 2048  # the planted duplicates
+    if mode > 0:
+        # the fix leaves at most the single maximum of each non-repeated row at 1.0
+        assert c["ones"] <= 4 * 12 * 2048 - c["repeated_rows"] + 64
+
+
+def test_long_context():
+    t = inputs.make("long", seed=0)
+    scale = 1.0 / math.sqrt(128)
+    got = run_gpu(t, causal=True, scale=scale, fix_mode=1, beta=4.0)
+    _check_groups(t, got, [(1, 15)], causal=True, scale=scale, mode=1, beta=4.0)
+    assert got["counters"]["nonfinite_rows"] == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_gqa_large_logits(mode):
+    t = inputs.make("gqa", seed=0)
+    scale = 1.0 / math.sqrt(128)
+    got = run_gpu(t, causal=True, scale=scale, fix_mode=mode, beta=2.0)
+    _check_groups(t, got, [(0, 3)], causal=True, scale=scale, mode=mode, beta=2.0)
+    assert got["counters"]["nonfinite_rows"] == 0
+    if mode == 0:
+        assert got["counters"]["ones"] >= 32 * 8192
+
+
+# ---------------------------------------------------------------- degenerate cases
+def test_underflow_probe_matches_emulation():
+    # Mode 1 with a repeated maximum of 200: beta*r_m pushes every exponent below FP32 range.
+    for logit, expect_nonfinite in ((200.0, True), (10.0, False)):
+        t = inputs.underflow_probe(1, 2, 128, 64, logit=logit)
+        got = run_gpu(t, causal=False, scale=0.125, fix_mode=1, beta=2.0, bwd=False)
+        q, k, v = (f64(t[n]) for n in ("q", "k", "v"))
+        emu = oracle.attn_fwd(q, k, v, scale=0.125, fix_mode=1, beta=2.0, emulate_bf16=True)
+        assert got["counters"] == emu["counters"]
+        assert (got["counters"]["nonfinite_rows"] == 256) == expect_nonfinite
+        if expect_nonfinite:
+            assert np.isnan(got["o"]).all()
+        else:
+            assert np.isfinite(got["o"]).all()
+        # mode 2 never underflows here
+        got2 = run_gpu(t, causal=False, scale=0.125, fix_mode=2, bwd=False)
+        assert got2["counters"]["nonfinite_rows"] == 0
+
+
+def test_counters_accumulate_and_are_optional():
+    t = to_dev(inputs.make("grid", seed=1))
+    cnt = pfa.new_counters()
+    for _ in range(2):
+        pfa.forward(t["q"], t["k"], t["v"], scale=0.125, fix_mode=1, counters=cnt)
+    o_nc, lse_nc = pfa.forward(t["q"], t["k"], t["v"], scale=0.125, fix_mode=1)
+    o_c, lse_c = pfa.forward(t["q"], t["k"], t["v"], scale=0.125, fix_mode=1,
+                             counters=pfa.new_counters())
+    torch.cuda.synchronize()
+    ref = oracle.attn_fwd(*(f64(t[n].cpu()) for n in ("q", "k", "v")), scale=0.125, fix_mode=1)
+    assert cnt.cpu().tolist() == [2 * ref["counters"][n] for n in
+                                  ("repeated_rows", "ones", "nonfinite_rows")]
+    assert torch.equal(o_nc, o_c) and torch.equal(lse_nc, lse_c)
+
+
+def test_invalid_arguments_raise():
+    t = to_dev(inputs.make("tiny"))
+    with pytest.raises(pfa.PfaError):
+        pfa.forward(t["q"], t["k"], t["v"], scale=0.125, fix_mode=1, beta=0.5)
+    with pytest.raises(ValueError):
+        pfa.forward(t["q"].float(), t["k"], t["v"], scale=0.125)
+    assert pfa.device_error() == 0
+
+
+def test_stream_and_autograd_wrapper():
+    t = to_dev(inputs.gaussian(1, 2, 2, 150, 64, std_qkv=0.5, seed=5))
+    q, k, v = (t[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o = pfa.StabilizedAttention.apply(q, k, v, True, 0.125, 1, 2.0, 1e-3)
+        o.backward(t["do"])
+    torch.cuda.synchronize()
+    ref = oracle_full({n: x.cpu() for n, x in t.items()}, causal=True, scale=0.125, fix_mode=1)
+    assert_fwd_close({"o": f64(o), "lse": ref["lse"]}, ref)
+    assert_bwd_close({"dq": f64(q.grad), "dk": f64(k.grad), "dv": f64(v.grad)}, ref)
