@@ -265,7 +265,9 @@ def run_gpu_arm(args):
     __graft_entry__.build()
     import precision_flash_attention_gb300 as pfa
 
-    w = WORKLOAD
+    w = dict(WORKLOAD)
+    if args.n:
+        w["N"] = args.n
     peaks = load_peaks()
     t = make_inputs(dev, w["B"], w["H"], w["N"], w["d"], seed=rank)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -291,6 +293,11 @@ def run_gpu_arm(args):
         torch.distributed.barrier()
     wall = time.perf_counter() - wall0
     assert pfa.device_error() == 0, "device error word set during the benchmark"
+    if args.kernels_only:
+        # Profiling run: the kernels above are all it launches (no sweep, copies or CPU work).
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
 
     mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
     ms = mean(res[head]["step_ms"])
@@ -408,6 +415,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mode", type=int, default=1, choices=[0, 1, 2])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--n", type=int, default=0, help="override the sequence length (profiling)")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="launch only the timed steps (for ncu captures); prints nothing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
