@@ -80,8 +80,8 @@ typedef struct pfa_counters {
  *   fix_mode 1: repeated rows m = beta*r_m if r_m > 0, 0 if r_m < 0, 2^-5 if
  *               r_m == 0; other rows m = r_m;
  *   fix_mode 2: repeated rows m = r_m + 2^-5; other rows m = r_m.
- * Pbar = exp(S - m) rounded to BF16, l = sum of those BF16 values,
- * O = (Pbar V) / l rounded to BF16, lse = m + ln(l) in FP32.
+ * Pbar = exp(S - m) in FP32, l = its row sum (FP32), O = (BF16(Pbar) V) / l
+ * rounded to BF16 (the product accumulates in FP32), lse = m + ln(l) in FP32.
  *   q [B,H_q,N,d], k, v [B,H_kv,N,d] (in); o [B,H_q,N,d], lse [B,H_q,N] (out).
  *   beta > 1 (mode 1; [PK] recommends 2..8; ignored otherwise).
  *   eps >= 0 finite: the tie tolerance ([PK] suggests 1e-3). It selects the rows

@@ -142,14 +142,17 @@ def attn_fwd_head(qh, kh, vh, *, causal=False, scale=None, fix_mode=0, beta=2.0,
 
     x = s - m[:, None]
     if emulate_bf16:
-        pbar = ftz32(bf16_rne(ftz32(np.exp(fp32(x))))).astype(np.float64)
+        p32 = ftz32(np.exp(fp32(x))).astype(np.float64)     # Pbar in FP32
+        pbar = ftz32(bf16_rne(p32)).astype(np.float64)      # its BF16 cast, the Pbar V operand
         pbar_bf16 = pbar
     else:
-        pbar = np.exp(x)
+        p32 = pbar = np.exp(x)
         pbar_bf16 = bf16_rne(fp32(pbar)).astype(np.float64)
     ones = (pbar_bf16 == 1.0).sum(axis=1)
 
-    l = pbar.sum(axis=1)
+    # l is the row sum of Pbar itself (before its BF16 cast), so lse = m + ln l keeps FP32
+    # accuracy and P = exp(S - lse) in the backward pass sums to one.
+    l = p32.sum(axis=1)
     obar = pbar @ vh
     with np.errstate(divide="ignore", invalid="ignore"):
         if emulate_bf16:

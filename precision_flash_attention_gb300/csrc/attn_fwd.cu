@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
           tmem_st_wait();
         }
 
-        // Pass 2: Pbar = exp(S - m) in FP32 -> BF16 into the P buffer; l sums the
-        // BF16 values that the MMA will see.
+        // Pass 2: Pbar = exp(S - m) in FP32 -> BF16 into the P buffer. l sums the
+        // FP32 Pbar, so lse = m + ln l stays exact to FP32 and the backward pass's
+        // P = exp(S - lse) is normalised.
         const float mlog2 = m_sh * kLog2e;
         const float thr = m1 - args.tau_raw;
         int cnt_tile = 0;
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
             const float p0 = ex2_approx(fmaf(x0, sl2, -mlog2));
             const float p1 = ex2_approx(fmaf(x1, sl2, -mlog2));
             pk[t] = pack_bf16x2(p0, p1);
-            ls[t & 1] += bf16lo_to_f32(pk[t]) + bf16hi_to_f32(pk[t]);
+            ls[t & 1] += p0 + p1;
           }
           const uint32_t prow = sbase + L::kP + (c4 >> 1) * L::kPanelBytes;
 #pragma unroll
