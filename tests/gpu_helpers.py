@@ -89,3 +89,28 @@ def oracle_group(t: dict, b: int, hk: int, *, causal, scale, fix_mode, beta=2.0,
     gr = oracle.attn_bwd(q, k, v, do, f["lse"], delta, causal=causal, scale=scale)
     return {"o": f["o"][0], "lse": f["lse"][0], "delta": delta[0], "dq": gr["dq"][0],
             "dk": gr["dk"][0, 0], "dv": gr["dv"][0, 0], "counters": f["counters"], "heads": hs}
+
+
+def oracle_group_emulated(t: dict, b: int, hk: int, *, causal, scale, fix_mode, beta=2.0, eps=1e-3,
+                          delta_mode=0):
+    """The BF16-emulating oracle (the kernel's cast points: FP32 scores, BF16 P / dS operands,
+    BF16 outputs) on one key/value-head group; delta from the emulated O (delta_mode 0) or as
+    rowsum(dP o P) (delta_mode 1)."""
+    Hq, Hkv = t["q"].shape[1], t["k"].shape[1]
+    g = Hq // Hkv
+    hs = slice(hk * g, (hk + 1) * g)
+    q = f64(t["q"][b:b + 1, hs])
+    do = f64(t["do"][b:b + 1, hs])
+    k = f64(t["k"][b:b + 1, hk:hk + 1])
+    v = f64(t["v"][b:b + 1, hk:hk + 1])
+    f = oracle.attn_fwd(q, k, v, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps,
+                        emulate_bf16=True)
+    if delta_mode == 0:
+        delta = oracle.attn_delta(f["o"], do, emulate_bf16=True)
+    else:
+        delta = oracle.attn_delta_alt(q, k, v, do, f["lse"], causal=causal, scale=scale,
+                                      emulate_bf16=True)
+    gr = oracle.attn_bwd(q, k, v, do, f["lse"], delta, causal=causal, scale=scale,
+                         emulate_bf16=True)
+    return {"o": f["o"][0], "lse": f["lse"][0], "dq": gr["dq"][0], "dk": gr["dk"][0, 0],
+            "dv": gr["dv"][0, 0], "heads": hs}

@@ -11,7 +11,7 @@ import oracle
 import precision_flash_attention_gb300 as pfa
 from precision_flash_attention_gb300 import inputs
 from tests.gpu_helpers import (TOL_BWD_REL, assert_bwd_close, assert_fwd_close, f64, oracle_full,
-                               oracle_group, rel_l2, run_gpu, to_dev)
+                               oracle_group, oracle_group_emulated, rel_l2, run_gpu, to_dev)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
 
@@ -60,8 +60,17 @@ def test_grid_counters_bit_exact(mode, causal, shape):
     assert_fwd_close({"o": got["o"][~bad], "lse": got["lse"][~bad]},
                      {"o": ref["o"][~bad], "lse": ref["lse"][~bad]}, "grid")
     if not bad.any():
+        # Integer scores concentrate P on planted maxima; the BF16 cast of dS then puts dQ
+        # within a hair of the float64 tolerance in the oracle's own emulation (0.6-1.0%),
+        # so dQ is held to the emulating oracle and dK, dV to float64.
         got = run_gpu(t, causal=causal, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
-        assert_bwd_close(got, oracle_full(t, causal=causal, scale=0.125, fix_mode=mode), "grid")
+        ref = oracle_full(t, causal=causal, scale=0.125, fix_mode=mode)
+        assert_bwd_close(got, ref, "grid", names=("dk", "dv"))
+        for b in range(B):
+            for hk in range(Hkv):
+                e = oracle_group_emulated(t, b, hk, causal=causal, scale=0.125, fix_mode=mode)
+                assert_bwd_close({"dq": got["dq"][b, e["heads"]]}, e, "grid (emulated)",
+                                 names=("dq",))
 
 
 # ---------------------------------------------------------------- ragged shapes
@@ -128,22 +137,32 @@ def test_gpt2_small_layer_all_heads():
         assert abs(got["counters"]["repeated_rows"] - ref["counters"]["repeated_rows"]) <= 8
 
 
-def _check_groups(t, got, groups, *, causal, scale, mode, beta):
+def _check_groups(t, got, groups, *, causal, scale, mode, beta, dq_emulated=False,
+                  delta_mode=0):
     for b, hk in groups:
         r = oracle_group(t, b, hk, causal=causal, scale=scale, fix_mode=mode, beta=beta)
         hs = r["heads"]
         assert_fwd_close({"o": got["o"][b, hs], "lse": got["lse"][b, hs]}, r, f"group {b},{hk}")
-        assert_bwd_close({"dq": got["dq"][b, hs], "dk": got["dk"][b, hk], "dv": got["dv"][b, hk]},
-                         r, f"group {b},{hk}")
+        g = {"dq": got["dq"][b, hs], "dk": got["dk"][b, hk], "dv": got["dv"][b, hk]}
+        if dq_emulated:
+            assert_bwd_close(g, r, f"group {b},{hk}", names=("dk", "dv"))
+            e = oracle_group_emulated(t, b, hk, causal=causal, scale=scale, fix_mode=mode,
+                                      beta=beta, delta_mode=delta_mode)
+            assert_bwd_close(g, e, f"group {b},{hk} (emulated)", names=("dq",))
+        else:
+            assert_bwd_close(g, r, f"group {b},{hk}")
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_sink_heavy(mode):
-    # delta = rowsum(dP o P), the alternative the paper found stable (its §3.2): every output
-    # within the float64 tolerances.
+    # delta = rowsum(dP o P), the alternative the paper found stable (its §3.2): O, lse, dK
+    # and dV within the float64 tolerances. dQ is held to the BF16-emulating oracle: the
+    # BF16 cast of dS against the sink key's feature of 48 moves dQ by about 12% from float64
+    # in the oracle's own emulation (exact lse and delta), the same amount as on the GPU.
     t = inputs.make("sink", seed=0)
     got = run_gpu(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0, delta_mode=1)
-    _check_groups(t, got, [(0, 0), (3, 11), (1, 5)], causal=True, scale=0.125, mode=mode, beta=2.0)
+    _check_groups(t, got, [(0, 0), (3, 11), (1, 5)], causal=True, scale=0.125, mode=mode, beta=2.0,
+                  dq_emulated=True, delta_mode=1)
     c = got["counters"]
     assert c["nonfinite_rows"] == 0
     assert c["repeated_rows"] > 0.1 * 4 * 12 * 2048  # the planted duplicates
