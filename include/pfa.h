@@ -51,7 +51,8 @@ enum {
   PFA_ERR_MISALIGNED = -2,  /* a pointer is not 16-byte aligned */
   PFA_ERR_UNSUPPORTED = -3, /* no sm_103 device current, or driver lacks TMA map encoding */
   PFA_ERR_LAUNCH = -4,      /* a CUDA launch or runtime call failed */
-  PFA_ERR_DEVICE = -5       /* pfa_device_error(): a kernel reported a failure */
+  PFA_ERR_DEVICE = -5,      /* pfa_device_error(): a kernel reported a failure */
+  PFA_ERR_TOO_LARGE = -6    /* pfa_attn_bwd_noalloc: problem exceeds its fixed buffer */
 };
 
 /* Device error word bits, as returned by pfa_device_error(). */
@@ -120,6 +121,28 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
                  const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
                  float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
                  pfa_stream_t stream);
+
+/* The same backward pass for callers that cannot allocate device memory (no
+ * counterpart in the paper; this is a deployment convenience). Some callers are
+ * not allowed to call cudaMalloc at all: runtimes that reserve all device memory
+ * up front in their own pool, real-time loops that cannot take cudaMalloc's
+ * implicit device synchronisation, or plugins that are handed only their input
+ * and output buffers. This entry point takes exactly the arguments of
+ * pfa_attn_bwd except dq_accum: the FP32 dQ accumulation buffer is a fixed
+ * library-owned array of 8,388,608 floats (32 MiB) that every GPU loading the
+ * library holds until the process exits. It allocates nothing.
+ *   - Limit: B * H_q * N * d must not exceed 8,388,608; larger problems return
+ *     PFA_ERR_TOO_LARGE before anything is launched (use pfa_attn_bwd instead).
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - All calls share the one array per device and it keeps the last call's
+ *     contents; each call zeroes it on `stream` first. Calls whose work overlaps
+ *     on the GPU (different streams without ordering between them) race on it:
+ *     order them on one stream or with events. */
+int pfa_attn_bwd_noalloc(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v,
+                         const pfa_bf16* dO, const float* lse, const float* delta, pfa_bf16* dq,
+                         pfa_bf16* dk, pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d,
+                         int causal, float scale, pfa_stream_t stream);
 
 /* Bytes of the dq_accum workspace pfa_attn_bwd needs: B*H_q*N*d*4 (0 on bad sizes). */
 size_t pfa_bwd_workspace_bytes(int B, int H_q, int N, int d);

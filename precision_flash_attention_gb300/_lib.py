@@ -18,11 +18,13 @@ _LIB = None
 
 PFA_OK = 0
 STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED",
-                -3: "PFA_ERR_UNSUPPORTED", -4: "PFA_ERR_LAUNCH", -5: "PFA_ERR_DEVICE"}
+                -3: "PFA_ERR_UNSUPPORTED", -4: "PFA_ERR_LAUNCH", -5: "PFA_ERR_DEVICE",
+                -6: "PFA_ERR_TOO_LARGE"}
 
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
-           "pfa_bwd_workspace_bytes", "pfa_status_string", "pfa_device_error")
+           "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
+           "pfa_device_error")
 
 
 class PfaError(RuntimeError):
@@ -53,6 +55,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_attn_delta_alt.restype = i
     lib.pfa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.pfa_attn_bwd.restype = i
+    lib.pfa_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.pfa_attn_bwd_noalloc.restype = i
     lib.pfa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.pfa_bwd_workspace_bytes.restype = sz
     lib.pfa_status_string.argtypes = [i]
@@ -150,6 +154,22 @@ def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, sca
                              _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, k.shape[1], N, d,
                              int(bool(causal)), float(scale), _stream(stream))
     _check(st, "pfa_attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, do, lse, delta, dq, dk, dv, *, causal: bool, scale: float,
+                     stream=None) -> None:
+    """pfa_attn_bwd_noalloc: the backward pass without a caller workspace, for callers that
+    may not allocate device memory; its dQ accumulation buffer is a fixed library-owned array
+    (B * H_q * N * d <= 8,388,608), shared by all calls on a device."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _bhnd(t, n)
+    _bhnd(lse, "lse", torch.float32, 3)
+    _bhnd(delta, "delta", torch.float32, 3)
+    B, Hq, N, d = q.shape
+    st = load().pfa_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, k.shape[1], N, d,
+                                     int(bool(causal)), float(scale), _stream(stream))
+    _check(st, "pfa_attn_bwd_noalloc")
 
 
 def device_error(clear: bool = False) -> int:

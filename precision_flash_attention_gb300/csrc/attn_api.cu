@@ -227,6 +227,7 @@ const char* pfa_status_string(int status) {
     case PFA_ERR_UNSUPPORTED: return "PFA_ERR_UNSUPPORTED: current device is not sm_103 or TMA encoding is unavailable";
     case PFA_ERR_LAUNCH: return "PFA_ERR_LAUNCH: a CUDA launch or runtime call failed";
     case PFA_ERR_DEVICE: return "PFA_ERR_DEVICE: a kernel reported a failure in the device error word";
+    case PFA_ERR_TOO_LARGE: return "PFA_ERR_TOO_LARGE: B*H_q*N*d exceeds the 8,388,608-value buffer of pfa_attn_bwd_noalloc";
     default: return "PFA_ERR_UNKNOWN";
   }
 }
