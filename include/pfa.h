@@ -150,6 +150,10 @@ size_t pfa_bwd_workspace_bytes(int B, int H_q, int N, int d);
 /* Human-readable name of a PFA_* status code (static string, never NULL). */
 const char* pfa_status_string(int status);
 
+/* Description of the most recent CUDA runtime error behind a PFA_ERR_LAUNCH
+ * returned to the calling thread ("no CUDA error" if there was none). */
+const char* pfa_last_error(void);
+
 /* Reads (and, if clear != 0, resets) the device error word of the current device.
  * Returns the PFA_DEVERR_* bits (>= 0) or a negative PFA_ERR_* code. This call
  * synchronises the current device. */

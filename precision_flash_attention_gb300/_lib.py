@@ -24,13 +24,16 @@ STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED"
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
            "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
-           "pfa_device_error")
+           "pfa_last_error", "pfa_device_error")
 
 
 class PfaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        detail = ""
+        if status == -4:  # PFA_ERR_LAUNCH: name the CUDA error behind it
+            detail = f" [{load().pfa_last_error().decode()}]"
+        super().__init__(f"{where}: {status_string(status)} ({status}){detail}")
 
 
 def library_path() -> str:
@@ -61,6 +64,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_bwd_workspace_bytes.restype = sz
     lib.pfa_status_string.argtypes = [i]
     lib.pfa_status_string.restype = ctypes.c_char_p
+    lib.pfa_last_error.argtypes = []
+    lib.pfa_last_error.restype = ctypes.c_char_p
     lib.pfa_device_error.argtypes = [i]
     lib.pfa_device_error.restype = i
     if path is None:

@@ -104,7 +104,14 @@ pfa::AttnShape shape(int B, int Hq, int Hkv, int N, int d, int causal, float sca
   return s;
 }
 
-int launched(cudaError_t e) { return e == cudaSuccess ? PFA_OK : PFA_ERR_LAUNCH; }
+// The most recent CUDA error seen by this thread's calls into the library.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int launched(cudaError_t e) {
+  if (e == cudaSuccess) return PFA_OK;
+  g_last_cuda_error = e;
+  return PFA_ERR_LAUNCH;
+}
 
 }  // namespace
 
@@ -206,7 +213,7 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
-  if (cudaMemsetAsync(dq_accum, 0, ws, st) != cudaSuccess) return PFA_ERR_LAUNCH;
+  if ((rc = launched(cudaMemsetAsync(dq_accum, 0, ws, st))) != PFA_OK) return rc;
   pfa::BwdArgs a;
   a.s = shape(B, H_q, H_kv, N, d, causal, scale);
   a.lse = lse;
@@ -230,6 +237,10 @@ const char* pfa_status_string(int status) {
     case PFA_ERR_TOO_LARGE: return "PFA_ERR_TOO_LARGE: B*H_q*N*d exceeds the 8,388,608-value buffer of pfa_attn_bwd_noalloc";
     default: return "PFA_ERR_UNKNOWN";
   }
+}
+
+const char* pfa_last_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
 }
 
 int pfa_device_error(int clear) {

@@ -1,7 +1,8 @@
 // Forward kernel: S = alpha Q K^T on tcgen05 (FP32 in TMEM), the online safe
 // softmax with the repeated-maximum tracker and the per-call shift rule,
-// Pbar = exp(S - m) in BF16, Obar += Pbar V on tcgen05 (FP32 in TMEM), then
-// O = Obar / l (BF16) and lse = m + ln l (FP32), plus the diagnostic counters.
+// Pbar = exp(S - m) in FP32 cast to BF16, Obar += Pbar V on tcgen05 (FP32 in
+// TMEM), then O = Obar / l (BF16) and lse = m + ln l (FP32), plus the
+// diagnostic counters.
 //
 // The method is the one analysed in Qiu & Yao, "Why Low-Precision Transformer
 // Training Fails: An Analysis on Flash Attention" (ICLR 2026), as summarised by
@@ -9,42 +10,44 @@
 // equations, and the fix of paper §4) and the bud-325 note of the same title
 // (Key claims, Method / Algorithm 1).
 //
-// CTA = one 128-row Q tile of one (batch, query head). 192 threads:
-//   warp 0      TMA producer (Q once, then K_j / V_j into a 2-stage ring)
+// CTA = two 128-row Q tiles (t = 0, 1) of one (batch, query head). 384 threads,
+// one warpgroup per role group (registers are granted per warpgroup):
+//   warp 0      TMA producer (Q0, Q1 once; then K_j and V_j into a stage ring)
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
-//   warps 2..5  softmax / correction / epilogue, one query row per thread
-//               (TMEM lane quarter = warp % 4)
-// TMEM: columns [0,128) hold S_j, columns [128, 128+d) hold Obar.
+//   warps 2, 3  idle
+//   warps 4..7  softmax of tile 0, warps 8..11 softmax of tile 1; one query row
+//               per thread (TMEM lane quarter = warp % 4)
+// TMEM (512 columns): S_t in [128 t, 128 t + 128), O_t in [256 + d t, 256 + d t + d).
+// Pbar_t (BF16) is written over the first 64 columns of S_t and is the TMEM A
+// operand of Obar_t += Pbar_t V.
+// The tensor core runs S0_j, PV1_{j-1}, S1_j, PV0_j, ... so that each tile's
+// softmax overlaps the other tile's two products.
 #include "pfa_device.cuh"
 
 namespace pfa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kEpsShift = 0.03125f;  // 2^-5
 
 template <int D>
 struct FwdLayout {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kTileBytes = kTile * D * 2;   // 128 rows x D bf16
   static constexpr int kPanelBytes = kTile * 128;    // 128 rows x 64 bf16
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kTileBytes;
+  static constexpr int kQ = 0;                       // + t * tile
+  static constexpr int kK = 2 * kTileBytes;          // + stage * tile
   static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kP = kV + kStages * kTileBytes;
-  static constexpr int kBars = kP + kTile * kTile * 2;
-  // barrier indices
+  static constexpr int kBars = kV + kStages * kTileBytes;
   static constexpr int bQFull = 0;
-  static constexpr int bKFull = 1;                  // + stage
-  static constexpr int bVFull = bKFull + kStages;   // + stage
-  static constexpr int bKVEmpty = bVFull + kStages; // + stage
-  static constexpr int bSFull = bKVEmpty + kStages;
-  static constexpr int bSFree = bSFull + 1;
-  static constexpr int bPFull = bSFree + 1;
-  static constexpr int bODone = bPFull + 1;
-  static constexpr int bDrain = bODone + 1;
+  static constexpr int bKVFull = 1;                   // + stage
+  static constexpr int bKVEmpty = bKVFull + kStages;  // + stage
+  static constexpr int bSFull = bKVEmpty + kStages;   // + tile
+  static constexpr int bPFull = bSFull + 2;           // + tile
+  static constexpr int bODone = bPFull + 2;           // + tile
+  static constexpr int bDrain = bODone + 2;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
@@ -52,7 +55,7 @@ struct FwdLayout {
 };
 
 template <int D, int MODE, bool CAUSAL, bool COUNT>
-__global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
   using L = FwdLayout<D>;
@@ -66,16 +69,20 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
 
   const AttnShape& sh = args.s;
   const int N = sh.N;
-  const int n_qt = (N + kTile - 1) / kTile;
+  const int n_kt = (N + kTile - 1) / kTile;   // key tiles == query tiles
+  const int n_pairs = (n_kt + 1) / 2;
   const int BHq = sh.B * sh.Hq;
   const int bh = blockIdx.x % BHq;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x / BHq);  // heaviest causal tiles first
-  const int q0 = qt * kTile;
+  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x / BHq);  // heaviest first
   const int b = bh / sh.Hq;
   const int h = bh % sh.Hq;
   const int bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
-  const int n_kt_all = (N + kTile - 1) / kTile;
-  const int n_kt = CAUSAL ? min(qt + 1, n_kt_all) : n_kt_all;
+  const int qt0 = 2 * pair;
+  const bool has1 = qt0 + 1 < n_kt;
+  // Last key tile each query tile visits (-1: the tile does not exist).
+  const int last0 = CAUSAL ? qt0 : n_kt - 1;
+  const int last1 = has1 ? (CAUSAL ? qt0 + 1 : n_kt - 1) : -1;
+  const int n_iter = max(last0, last1) + 1;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -87,157 +94,194 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
     if (sbase & 1023u) atomicOr(args.err, PFA_DEVERR_SMEM_ALIGN);
     mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::bKFull + s), 1);
-      mbar_init(bar(L::bVFull + s), 1);
+      mbar_init(bar(L::bKVFull + s), 1);
       mbar_init(bar(L::bKVEmpty + s), 1);
     }
-    mbar_init(bar(L::bSFull), 1);
-    mbar_init(bar(L::bSFree), 4);
-    mbar_init(bar(L::bPFull), 4);
-    mbar_init(bar(L::bODone), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::bSFull + t), 1);
+      mbar_init(bar(L::bPFull + t), 4);
+      mbar_init(bar(L::bODone + t), 1);
+    }
     mbar_init(bar(L::bDrain), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;
-  const uint32_t tO = tmem + 128;
-
-  if (*abort_flag == 0) {
+  // Register split per warpgroup. The block is launched with 168 registers per
+  // thread (384 x 168 = 64512). Warpgroup 0 (producer, MMA, two idle warps) drops
+  // to 56 and the two softmax warpgroups rise to 224: 128 x 56 + 256 x 224 =
+  // 64512. Each group returns to 168 before the common teardown (the same sum).
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    if (*abort_flag == 0) {
     if (warp == 0) {
       // ---------------- TMA producer ----------------
       if (lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        mbar_arrive_expect_tx(bar(L::bQFull), L::kTileBytes);
-        for (int p = 0; p < D / 64; ++p)
-          tma_load_3d(sbase + L::kQ + p * L::kPanelBytes, &tmQ, bar(L::bQFull), p * 64, q0, bh);
+        mbar_arrive_expect_tx(bar(L::bQFull), (has1 ? 2 : 1) * L::kTileBytes);
+        for (int t = 0; t < (has1 ? 2 : 1); ++t)
+          for (int p = 0; p < D / 64; ++p)
+            tma_load_3d(sbase + L::kQ + t * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                        bar(L::bQFull), p * 64, (qt0 + t) * kTile, bh);
         int issued = 0;
-        for (int j = 0; j < n_kt; ++j) {
+        for (int j = 0; j < n_iter; ++j) {
           const int s = j % L::kStages;
           const uint32_t ph = (j / L::kStages) & 1;
           if (!wait_thread(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
           issued = j + 1;
-          mbar_arrive_expect_tx(bar(L::bKFull + s), L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p)
+          mbar_arrive_expect_tx(bar(L::bKVFull + s), 2 * L::kTileBytes);
+          for (int p = 0; p < D / 64; ++p) {
             tma_load_3d(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                        bar(L::bKFull + s), p * 64, j * kTile, bh_kv);
-          mbar_arrive_expect_tx(bar(L::bVFull + s), L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p)
+                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
             tma_load_3d(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                        bar(L::bVFull + s), p * 64, j * kTile, bh_kv);
+                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
+          }
         }
         // Drain: every issued copy has landed before shared memory is released.
         wait_drain(bar(L::bQFull), 0, args.err);
-        for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j) {
-          const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          wait_drain(bar(L::bKFull + s), ph, args.err);
-          wait_drain(bar(L::bVFull + s), ph, args.err);
-        }
+        for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
+          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, args.err);
       }
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
       if (lane == 0) {
         constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
         constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-        bool ok = wait_thread(bar(L::bQFull), 0, ctl);
-        auto issue_s = [&](int j) {
-          const int s = j % L::kStages;
-          tc_fence_after();
+        auto issue_s = [&](int t, int s) {
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            const uint64_t da = sdesc_sw128(sbase + L::kQ + koff, 16, 1024);
-            const uint64_t db = sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024);
-            umma_bf16(tS, da, db, idS, kk > 0);
+            umma_bf16(tmem + 128 * t, sdesc_sw128(sbase + L::kQ + t * L::kTileBytes + koff, 16, 1024),
+                      sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
           }
-          umma_commit(bar(L::bSFull));
+          umma_commit(bar(L::bSFull + t));
         };
-        if (ok) ok = wait_thread(bar(L::bKFull + 0), 0, ctl);
-        if (ok) issue_s(0);
-        for (int j = 0; ok && j < n_kt; ++j) {
+        // Obar_t (+)= Pbar_t V_j; Pbar_t is columns [0, 64) of S_t, 8 columns per K step.
+        auto issue_pv = [&](int t, int s, int j) {
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_tmem_a(tmem + 256 + D * t, tmem + 128 * t + 8 * kk,
+                             sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
+                                         L::kPanelBytes, 1024),
+                             idPV, (j > 0 || kk > 0) ? 1u : 0u);
+        };
+        bool ok = wait_thread(bar(L::bQFull), 0, ctl);
+        for (int j = 0; ok && j < n_iter; ++j) {
           const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          if (j + 1 < n_kt) {
-            const int s1 = (j + 1) % L::kStages;
-            const uint32_t ph1 = ((j + 1) / L::kStages) & 1;
-            if (!(ok = wait_thread(bar(L::bKFull + s1), ph1, ctl))) break;
-            if (!(ok = wait_thread(bar(L::bSFree), j & 1, ctl))) break;
-            issue_s(j + 1);
-          }
-          if (!(ok = wait_thread(bar(L::bPFull), j & 1, ctl))) break;
-          if (!(ok = wait_thread(bar(L::bVFull + s), ph, ctl))) break;
+          if (!(ok = wait_thread(bar(L::bKVFull + s), (j / L::kStages) & 1, ctl))) break;
+          const bool act0 = j <= last0, act1 = j <= last1;
           tc_fence_after();
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t da =
-                sdesc_sw128(sbase + L::kP + (kk >> 2) * L::kPanelBytes + (kk & 3) * 32, 16, 1024);
-            const uint64_t db =
-                sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048, L::kPanelBytes, 1024);
-            umma_bf16(tO, da, db, idPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (act0) issue_s(0, s);
+          if (j > 0 && j - 1 <= last1) {
+            if (!(ok = wait_thread(bar(L::bPFull + 1), (j - 1) & 1, ctl))) break;
+            tc_fence_after();
+            const int sp = (j - 1) % L::kStages;
+            issue_pv(1, sp, j - 1);
+            umma_commit(bar(L::bKVEmpty + sp));
+            if (j - 1 == last1) umma_commit(bar(L::bODone + 1));
           }
-          umma_commit(bar(L::bKVEmpty + s));
-          umma_commit(bar(L::bODone));
+          if (act1) issue_s(1, s);
+          if (act0) {
+            if (!(ok = wait_thread(bar(L::bPFull + 0), j & 1, ctl))) break;
+            tc_fence_after();
+            issue_pv(0, s, j);
+            if (j == last0) umma_commit(bar(L::bODone + 0));
+            if (!act1) umma_commit(bar(L::bKVEmpty + s));
+          }
+        }
+        if (ok && last1 == n_iter - 1) {
+          const int j = n_iter - 1;
+          if ((ok = wait_thread(bar(L::bPFull + 1), j & 1, ctl))) {
+            tc_fence_after();
+            issue_pv(1, j % L::kStages, j);
+            umma_commit(bar(L::bKVEmpty + j % L::kStages));
+            umma_commit(bar(L::bODone + 1));
+          }
         }
         // Drain: no MMA may still read shared memory or write TMEM at teardown.
         umma_commit(bar(L::bDrain));
         wait_drain(bar(L::bDrain), 0, args.err);
       }
-    } else {
+    }
+    }
+    __syncwarp();
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    if (*abort_flag == 0) {
       // ---------------- softmax warps ----------------
+      const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+      const int last = t ? last1 : last0;
       const uint32_t quarter = warp & 3;
       const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
+      const int q0 = (qt0 + t) * kTile;
       const int qrow = q0 + r;
       const uint32_t lane_off = (quarter * 32u) << 16;
+      const uint32_t tS = tmem + 128 * t + lane_off;
+      const uint32_t tO = tmem + 256 + D * t + lane_off;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
 
       float m1 = -INFINITY, m2 = -INFINITY;  // running top-2 of raw scores
       float m_sh = -INFINITY;                // current shift, natural units
-      float l = 0.f;
+      float l0 = 0.f, l1 = 0.f;              // row sum of Pbar (two partial sums)
       int cnt = 0;                           // entries within tau of m1 (raw)
       bool ok = true;
 
-      for (int j = 0; j < n_kt; ++j) {
+      for (int j = 0; j <= last; ++j) {
         const int k0 = j * kTile;
         const bool need_mask = (CAUSAL && k0 + kTile > q0) || (k0 + kTile > N);
-        if (!(ok = wait_warp(bar(L::bSFull), j & 1, ctl))) break;
+        if (!(ok = wait_warp(bar(L::bSFull + t), j & 1, ctl))) break;
         tc_fence_after();
-
-        // Pass 1: tile maximum (and second maximum) over visible keys.
-        float a1[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        float a2[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(tS + lane_off + c4 * 32, v);
-          tmem_ld_wait32(v);
+        uint32_t v[128];
+        tmem_ld64(tS, v);
+        tmem_ld64(tS + 64, v + 64);
+        tmem_ld_wait64(v);
+        tmem_ld_wait64(v + 64);
+        if (need_mask) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            float x = __uint_as_float(v[t]);
-            if (need_mask) {
-              const int key = k0 + c4 * 32 + t;
-              const bool vis = key < N && (!CAUSAL || key <= qrow);
-              x = vis ? x : -INFINITY;
-            }
-            if (kTies) a2[t & 3] = fmaxf(a2[t & 3], fminf(a1[t & 3], x));
-            a1[t & 3] = fmaxf(a1[t & 3], x);
+          for (int c = 0; c < kTile; ++c) {
+            const int key = k0 + c;
+            if (!(key < N && (!CAUSAL || key <= qrow))) v[c] = __float_as_uint(-INFINITY);
           }
         }
-        float t1 = a1[0], t2 = a2[0];
+        // Tile maximum.
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-        for (int i = 1; i < 4; ++i) {
-          if (kTies) t2 = fmaxf(fmaxf(t2, a2[i]), fminf(t1, a1[i]));
-          t1 = fmaxf(t1, a1[i]);
+        for (int c = 0; c < kTile; c += 8) {
+          a0 = fmax3(a0, __uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
+          a1 = fmax3(a1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+          a2 = fmax3(a2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+          a3 = fmax3(a3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+        }
+        const float t1 = fmax3(fmaxf(a0, a1), a2, a3);
+        // Second maximum (with multiplicity). A tile whose maximum stays below
+        // the running maximum contributes only that maximum to the top-2, so the
+        // sweep is needed only where a lane's maximum rises or ties.
+        if (kTies) {
+          float t2 = -INFINITY;
+          if (__any_sync(0xFFFFFFFFu, t1 >= m1)) {
+            float b0 = -INFINITY, b1 = -INFINITY;
+            int eq = 0;
+#pragma unroll
+            for (int c = 0; c < kTile; c += 2) {
+              const float x0 = __uint_as_float(v[c]), x1 = __uint_as_float(v[c + 1]);
+              const bool lt0 = x0 < t1, lt1 = x1 < t1;
+              eq += (lt0 ? 0 : 1) + (lt1 ? 0 : 1);
+              b0 = fmaxf(b0, lt0 ? x0 : -INFINITY);
+              b1 = fmaxf(b1, lt1 ? x1 : -INFINITY);
+            }
+            t2 = eq >= 2 ? t1 : fmaxf(b0, b1);
+          }
+          m2 = fmax3(m2, t2, fminf(m1, t1));
         }
         const float m1_old = m1;
-        if (kTies) m2 = fmaxf(fmaxf(m2, t2), fminf(m1, t1));
         m1 = fmaxf(m1, t1);
 
         // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
@@ -252,95 +296,77 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         }
         const bool changed = (j > 0) && (m_new != m_sh);
         const float corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
-        l *= corr;
+        l0 *= corr;
+        l1 *= corr;
         m_sh = m_new;
 
-        // The previous P.V must be complete before Obar is rescaled or the P
-        // buffer is overwritten.
-        if (j > 0) {
-          if (!(ok = wait_warp(bar(L::bODone), (j - 1) & 1, ctl))) break;
-          tc_fence_after();
-        }
+        // Rescale Obar where the shift moved. S_t of this tile was committed after
+        // the previous P.V of this tile, so that product has completed.
         if (__any_sync(0xFFFFFFFFu, changed)) {
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tO + lane_off + c, v);
-            tmem_ld_wait32(v);
+            uint32_t o[32];
+            tmem_ld32(tO + c, o);
+            tmem_ld_wait32(o);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * corr);
-            tmem_st32(tO + lane_off + c, v);
+            for (int u = 0; u < 32; u += 2) {
+              float y0 = __uint_as_float(o[u]), y1 = __uint_as_float(o[u + 1]);
+              mul2(y0, y1, corr);
+              o[u] = __float_as_uint(y0);
+              o[u + 1] = __float_as_uint(y1);
+            }
+            tmem_st32(tO + c, o);
           }
-          tmem_st_wait();
         }
 
-        // Pass 2: Pbar = exp(S - m) in FP32 -> BF16 into the P buffer. l sums the
-        // FP32 Pbar, so lse = m + ln l stays exact to FP32 and the backward pass's
-        // P = exp(S - lse) is normalised.
-        const float mlog2 = m_sh * kLog2e;
+        // Pbar = exp(S - m) in FP32; l sums it; the BF16 cast goes to TMEM over S.
+        const float nml2 = -m_sh * kLog2e;
         const float thr = m1 - args.tau_raw;
         int cnt_tile = 0;
-        float ls[2] = {0.f, 0.f};
-#pragma unroll 1
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(tS + lane_off + c4 * 32, v);
-          tmem_ld_wait32(v);
-          if (c4 == 3) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::bSFree));
-          }
-          uint32_t pk[16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            float x0 = __uint_as_float(v[2 * t]);
-            float x1 = __uint_as_float(v[2 * t + 1]);
-            if (need_mask) {
-              const int key = k0 + c4 * 32 + 2 * t;
-              const bool vis0 = key < N && (!CAUSAL || key <= qrow);
-              const bool vis1 = key + 1 < N && (!CAUSAL || key + 1 <= qrow);
-              x0 = vis0 ? x0 : -INFINITY;
-              x1 = vis1 ? x1 : -INFINITY;
-            }
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float x0 = __uint_as_float(v[64 * half + 2 * u]);
+            const float x1 = __uint_as_float(v[64 * half + 2 * u + 1]);
             if (COUNT) cnt_tile += (x0 >= thr) + (x1 >= thr);
-            const float p0 = ex2_approx(fmaf(x0, sl2, -mlog2));
-            const float p1 = ex2_approx(fmaf(x1, sl2, -mlog2));
-            pk[t] = pack_bf16x2(p0, p1);
-            ls[t & 1] += p0 + p1;
+            float y0, y1;
+            fma2(y0, y1, x0, x1, sl2, nml2);
+            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            add2(l0, l1, p0, p1);
+            pk[u] = pack_bf16x2(p0, p1);
           }
-          const uint32_t prow = sbase + L::kP + (c4 >> 1) * L::kPanelBytes;
-#pragma unroll
-          for (int qd = 0; qd < 4; ++qd)
-            st_shared_v4(prow + sw128_offset(r, (c4 & 1) * 4 + qd), pk[4 * qd], pk[4 * qd + 1],
-                         pk[4 * qd + 2], pk[4 * qd + 3]);
+          tmem_st32(tS + 32 * half, pk);
         }
-        l += ls[0] + ls[1];
         if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bPFull));
+        if (lane == 0) mbar_arrive(bar(L::bPFull + t));
       }
 
       // ---------------- epilogue ----------------
-      if (ok && n_kt > 0) ok = wait_warp(bar(L::bODone), (n_kt - 1) & 1, ctl);
-      if (ok) {
+      if (ok && last >= 0) ok = wait_warp(bar(L::bODone + t), 0, ctl);
+      if (ok && last >= 0) {
         tc_fence_after();
+        const float l = l0 + l1;
         const bool row_ok = qrow < N;
         const float inv_l = 1.f / l;
         __nv_bfloat16* orow =
             reinterpret_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tO + lane_off + c, v);
-          tmem_ld_wait32(v);
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          tmem_ld_wait32(o);
           uint32_t pk[16];
 #pragma unroll
-          for (int t = 0; t < 16; ++t)
-            pk[t] = pack_bf16x2(__uint_as_float(v[2 * t]) * inv_l,
-                                __uint_as_float(v[2 * t + 1]) * inv_l);
+          for (int u = 0; u < 16; ++u) {
+            float y0 = __uint_as_float(o[2 * u]), y1 = __uint_as_float(o[2 * u + 1]);
+            mul2(y0, y1, inv_l);
+            pk[u] = pack_bf16x2(y0, y1);
+          }
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
@@ -374,6 +400,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
         }
       }
     }
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
   }
 
   tc_fence_before();
@@ -381,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, (D == 64 ? 2 : 1))
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -392,8 +419,8 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = attn_fwd_kernel<D, MODE, CAUSAL, COUNT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const int n_qt = (a.s.N + kTile - 1) / kTile;
-  const dim3 grid(static_cast<unsigned>(n_qt) * a.s.B * a.s.Hq);
+  const int n_kt = (a.s.N + kTile - 1) / kTile;
+  const dim3 grid(static_cast<unsigned>((n_kt + 1) / 2) * a.s.B * a.s.Hq);
   kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }

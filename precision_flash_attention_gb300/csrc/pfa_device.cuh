@@ -40,6 +40,36 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed FP32x2 arithmetic: two lanes of work per instruction.
+__device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, float a, float b) {
+  asm("{\n\t.reg .b64 xa, aa, ba, ya;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 aa, {%4, %4};\n\tmov.b64 ba, {%5, %5};\n\t"
+      "fma.rn.f32x2 ya, xa, aa, ba;\n\tmov.b64 {%0, %1}, ya;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a), "f"(b));
+}
+__device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
+  asm("{\n\t.reg .b64 sa, xa;\n\t"
+      "mov.b64 sa, {%0, %1};\n\tmov.b64 xa, {%2, %3};\n\t"
+      "add.rn.f32x2 sa, sa, xa;\n\tmov.b64 {%0, %1}, sa;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+__device__ __forceinline__ void mul2(float& y0, float& y1, float a) {
+  asm("{\n\t.reg .b64 ya, aa;\n\t"
+      "mov.b64 ya, {%0, %1};\n\tmov.b64 aa, {%2, %2};\n\t"
+      "mul.rn.f32x2 ya, ya, aa;\n\tmov.b64 {%0, %1}, ya;\n\t}"
+      : "+f"(y0), "+f"(y1)
+      : "f"(a));
+}
+
 // Two FP32 values -> packed BF16x2 (round to nearest even); `lo` goes to bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -209,6 +239,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A is read from tensor memory (one row per lane,
+// two BF16 values per 32-bit column, lower K index in the low half).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -285,6 +327,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       PFA_S8(0), PFA_S8(8), PFA_S8(16), PFA_S8(24)
       : "memory");
+}
+
+#define PFA_R64 PFA_R8(0), PFA_R8(8), PFA_R8(16), PFA_R8(24), PFA_R8(32), PFA_R8(40), PFA_R8(48), PFA_R8(56)
+#define PFA_W64 PFA_W8(0), PFA_W8(8), PFA_W8(16), PFA_W8(24), PFA_W8(32), PFA_W8(40), PFA_W8(48), PFA_W8(56)
+
+// 32 lanes x 64 consecutive 32-bit columns into r[0..63].
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
+      "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : PFA_R64
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait64(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : PFA_W64 : : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() {
