@@ -250,6 +250,11 @@ def cpu_baseline(sample_heads=48, seed=0):
             "seconds": dt}
 
 
+def _progress(args, msg):
+    if args.progress:
+        print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
 def run_gpu_arm(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -275,7 +280,9 @@ def run_gpu_arm(args):
     steps = {m: Step(t, causal=w["causal"], scale=w["scale"], fix_mode=m, beta=w["beta"],
                      eps=w["eps"]) for m in sorted({0, head})}
     for m in steps:
+        _progress(args, f"warm-up mode {m}")
         time_step(steps[m], 1, args.warmup, flush)
+        _progress(args, f"warm-up mode {m} done, device error word {pfa.device_error()}")
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -283,11 +290,15 @@ def run_gpu_arm(args):
     res = {m: {"fwd_ms": [], "delta_ms": [], "bwd_ms": [], "step_ms": []} for m in steps}
     wall0 = time.perf_counter()
     with ClockSampler(local) as clk:
-        for _ in range(args.steps):
+        for it in range(args.steps):
             for m in steps:
                 r = time_step(steps[m], 1, 0, flush)
                 for k2 in r:
                     res[m][k2] += r[k2]
+                if args.progress:
+                    err = pfa.device_error()
+                    _progress(args, f"step {it} mode {m}: {r['step_ms'][0]:.3f} ms, error word {err}"
+                                    + (f", first timeout at {pfa.device_error_site()}" if err else ""))
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -334,10 +345,12 @@ def run_gpu_arm(args):
                 if head != 0 else None)
 
     sweep = {}
+    _progress(args, f"timed steps done: {ms:.3f} ms per step")
     if args.sweep and rank == 0:
         for n_s in (2048, 4096, 8192):
             ts = make_inputs(dev, B, H, n_s, d, seed=1)
             for m in sorted({0, head}):
+                _progress(args, f"sweep N={n_s} mode {m}")
                 st = Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
                 r = time_step(st, max(3, args.steps // 2), 2, flush)
                 fm, bm, sm = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms", "step_ms"))
@@ -348,6 +361,7 @@ def run_gpu_arm(args):
                     "total_tflops": tot, "total_frac_bf16_peak": tot / peak}
             del ts
 
+    _progress(args, f"sweep done, device error word {pfa.device_error()}")
     e2e = None
     if rank == 0:
         e_ms, h2d, d2h = e2e_time(steps[head], max(3, args.steps // 2), args.warmup, flush)
@@ -359,6 +373,7 @@ def run_gpu_arm(args):
         if world > 1:
             torch.distributed.destroy_process_group()
         return
+    _progress(args, "e2e done; CPU baseline")
     cpu = cpu_baseline(sample_heads=48)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -416,6 +431,7 @@ def main():
     ap.add_argument("--mode", type=int, default=1, choices=[0, 1, 2])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--n", type=int, default=0, help="override the sequence length (profiling)")
+    ap.add_argument("--progress", action="store_true", help="log each stage to stderr")
     ap.add_argument("--kernels-only", action="store_true",
                     help="launch only the timed steps (for ncu captures); prints nothing")
     args = ap.parse_args()

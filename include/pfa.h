@@ -159,6 +159,14 @@ const char* pfa_last_error(void);
  * synchronises the current device. */
 int pfa_device_error(int clear);
 
+/* Where the first bounded wait that gave up (PFA_DEVERR_TIMEOUT) since the last
+ * pfa_device_error(1) was: 0 if none, else kernel id in bits 56-59 (1 forward,
+ * 2 backward, 3 delta via dP o P), bit 55 set for a teardown (drain) wait,
+ * bit 54 the awaited phase parity, bits 32-53 the barrier's byte offset in the
+ * kernel's shared memory, bits 0-31 blockIdx.x. Negative: a PFA_ERR_* code.
+ * Synchronises the current device. */
+long long pfa_device_error_site(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED"
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
            "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
-           "pfa_last_error", "pfa_device_error")
+           "pfa_last_error", "pfa_device_error", "pfa_device_error_site")
 
 
 class PfaError(RuntimeError):
@@ -66,6 +66,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_status_string.restype = ctypes.c_char_p
     lib.pfa_last_error.argtypes = []
     lib.pfa_last_error.restype = ctypes.c_char_p
+    lib.pfa_device_error_site.argtypes = []
+    lib.pfa_device_error_site.restype = ctypes.c_longlong
     lib.pfa_device_error.argtypes = [i]
     lib.pfa_device_error.restype = i
     if path is None:
@@ -183,3 +185,15 @@ def device_error(clear: bool = False) -> int:
     if st < 0:
         raise PfaError(st, "pfa_device_error")
     return st
+
+
+def device_error_site() -> dict | None:
+    """pfa_device_error_site, decoded: where the first timed-out wait was (None if none)."""
+    w = int(load().pfa_device_error_site())
+    if w < 0:
+        raise PfaError(w, "pfa_device_error_site")
+    if w == 0:
+        return None
+    return {"kernel": {1: "forward", 2: "backward", 3: "delta_alt"}.get((w >> 56) & 15, "?"),
+            "drain": bool((w >> 55) & 1), "parity": (w >> 54) & 1,
+            "barrier_offset": (w >> 32) & 0x3FFFFF, "block": w & 0xFFFFFFFF}

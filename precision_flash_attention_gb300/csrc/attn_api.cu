@@ -12,6 +12,8 @@ namespace {
 
 // Device error word: kernels OR PFA_DEVERR_* bits into it instead of trapping.
 __device__ int g_pfa_device_error;
+// Where the first bounded wait gave up since the last clear (0 if none).
+__device__ unsigned long long g_pfa_device_error_site;
 
 constexpr int kMaxDevices = 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -22,6 +24,7 @@ struct DeviceState {
   bool ready = false;
   bool supported = false;
   int* err = nullptr;  // device address of g_pfa_device_error on this device
+  unsigned long long* site = nullptr;  // device address of g_pfa_device_error_site
 };
 
 std::mutex g_mu;
@@ -46,6 +49,8 @@ int current_device(DeviceState** out) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_pfa_device_error) != cudaSuccess) return PFA_ERR_LAUNCH;
       st.err = static_cast<int*>(p);
+      if (cudaGetSymbolAddress(&p, g_pfa_device_error_site) != cudaSuccess) return PFA_ERR_LAUNCH;
+      st.site = static_cast<unsigned long long*>(p);
     }
     if (!g_encode_tried) {
       g_encode_tried = true;
@@ -142,6 +147,7 @@ int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf
   a.lse = lse;
   a.counters = reinterpret_cast<long long*>(counters);
   a.err = dev->err;
+  a.err_site = dev->site;
   a.fix_mode = fix_mode;
   a.beta = fix_mode == 1 ? beta : 2.f;
   a.eps_raw = ties ? eps / scale : 0.f;
@@ -183,6 +189,7 @@ int pfa_attn_delta_alt(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
   a.lse = lse;
   a.delta = delta;
   a.err = dev->err;
+  a.err_site = dev->site;
   return launched(pfa::launch_delta_alt(tq, tk, tv, tdo, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -222,6 +229,7 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   a.dk = dk;
   a.dv = dv;
   a.err = dev->err;
+  a.err_site = dev->site;
   if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, a, st))) != PFA_OK) return rc;
   return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
 }
@@ -252,9 +260,23 @@ int pfa_device_error(int clear) {
   if (cudaMemcpyFromSymbol(&word, g_pfa_device_error, sizeof(int)) != cudaSuccess) return PFA_ERR_LAUNCH;
   if (clear) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_pfa_device_error, &zero, sizeof(int)) != cudaSuccess) return PFA_ERR_LAUNCH;
+    const unsigned long long zero64 = 0;
+    if (cudaMemcpyToSymbol(g_pfa_device_error, &zero, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_pfa_device_error_site, &zero64, sizeof(zero64)) != cudaSuccess)
+      return PFA_ERR_LAUNCH;
   }
   return word;
+}
+
+long long pfa_device_error_site(void) {
+  DeviceState* dev = nullptr;
+  int rc = current_device(&dev);
+  if (rc != PFA_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PFA_ERR_LAUNCH;
+  unsigned long long site = 0;
+  if (cudaMemcpyFromSymbol(&site, g_pfa_device_error_site, sizeof(site)) != cudaSuccess)
+    return PFA_ERR_LAUNCH;
+  return static_cast<long long>(site & 0x7FFFFFFFFFFFFFFFull);
 }
 
 }  // extern "C"

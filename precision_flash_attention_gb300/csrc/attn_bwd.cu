@@ -2,39 +2,53 @@
 // query heads that share the key/value head and over the query tiles, with all
 // five products on tcgen05 (FP32 accumulators in TMEM):
 //   S^T  = K Q^T              P^T  = exp(alpha S^T - lse)      (recomputed)
-//   dP^T = V dO^T             dS^T = alpha P^T o (dP^T - delta)
+//   dP^T = V dO^T             dS^T = P^T o (dP^T - delta)      (alpha applied at the end)
 //   dV  += P^T dO             dK  += dS^T Q                    (stay in TMEM: no atomics)
-//   dQ   = dS K               -> FP32 reduce-add into the dQ workspace
+//   dQ   = dS K               -> alpha dQ reduce-added into the FP32 workspace
 // which is the backward pass of the priors.kr post "BF16 플래시 어텐션은 왜 수천
 // 스텝 뒤에 무너질까" (equations: dS = alpha P o (dP - delta), dQ = dS K) with the
 // standard dK / dV products. The fix of paper §4 does not change the backward
 // pass (priors.kr, the fix paragraph; bud-325 note, Results): P is recomputed
 // from the saved lse whatever shift the forward pass used.
 //
-// 192 threads: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2..5
-// one key row per thread for S^T / dP^T and one query row per thread for dQ.
+// 384 threads in three warpgroups: warp 0 TMA producer, warp 1 TMEM owner and
+// tcgen05.mma issuer, warps 2-3 idle; warps 4-11 compute. Compute warp w owns
+// TMEM lane quarter w % 4 (32 keys) and query half (w - 4) / 4 (64 queries).
+// P^T and dS^T are cast to BF16 and written back into TMEM over S^T and dP^T
+// (each query half over its own input columns), where they are the A operands of
+// dV and dK; dS^T also goes to a 128B-swizzled
+// shared buffer that the dQ product reads as its (M = queries) A operand.
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d),
-// dQ [384,448) for d = 64 and aliased onto S^T for d = 128.
+// dQ [384,448) for d = 64 and over dP^T [128,256) for d = 128.
+// Tensor-core order per query tile: S^T, dP^T, dV, dK, dQ; the P phase of the
+// compute warps overlaps dP^T and the dS phase overlaps dV.
 #include "pfa_device.cuh"
 
 namespace pfa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// P^T and dS^T (BF16, two per 32-bit column) are written by each query half into
+// the first 32 columns of that half's own 64 FP32 input columns, so one half never
+// overwrites values the other half has yet to load. Query step kk (16 queries,
+// 8 columns) therefore sits at column 8 kk for kk < 4 and 32 + 8 kk after.
+__host__ __device__ constexpr uint32_t packed_col(int kk) {
+  return 8u * static_cast<uint32_t>(kk) + (kk >= 4 ? 32u : 0u);
+}
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kStages = 2;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kPanelBytes = kTile * 128;
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;                // + stage * tile
   static constexpr int kDO = kQ + kStages * kTileBytes;     // + stage * tile
-  static constexpr int kP = kDO + kStages * kTileBytes;     // P^T  [keys][queries] bf16
-  static constexpr int kDS = kP + kTile * kTile * 2;        // dS^T [keys][queries] bf16
-  static constexpr int kLse = kDS + kTile * kTile * 2;      // 2 slots x 128 floats (scaled by log2 e)
+  static constexpr int kDS = kDO + kStages * kTileBytes;    // dS^T [keys][queries] bf16, 2 panels
+  static constexpr int kLse = kDS + kTile * kTile * 2;      // 2 slots x 128 floats (x log2 e)
   static constexpr int kDelta = kLse + 2 * kTile * 4;       // 2 slots x 128 floats
   static constexpr int kBars = kDelta + 2 * kTile * 4;
   static constexpr int bKVFull = 0;
@@ -42,22 +56,22 @@ struct BwdLayout {
   static constexpr int bQEmpty = bQFull + kStages;  // + stage
   static constexpr int bSFull = bQEmpty + kStages;
   static constexpr int bDPFull = bSFull + 1;
-  static constexpr int bSTFree = bDPFull + 1;
-  static constexpr int bDPFree = bSTFree + 1;
-  static constexpr int bPReady = bDPFree + 1;
+  static constexpr int bPReady = bDPFull + 1;
   static constexpr int bDSReady = bPReady + 1;
-  static constexpr int bPDSFree = bDSReady + 1;
-  static constexpr int bDQFull = bPDSFree + 1;
+  static constexpr int bDQFull = bDSReady + 1;
   static constexpr int bDQFree = bDQFull + 1;
-  static constexpr int bLse = bDQFree + 1;          // + slot (2): lse/delta staged
+  static constexpr int bLse = bDQFree + 1;          // + slot (2)
   static constexpr int bMMADone = bLse + 2;
   static constexpr int bDrain = bMMADone + 1;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bRegs = bDrain + 1;          // the compute warps hold their registers
+  static constexpr int kNumBars = bRegs + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-  static constexpr uint32_t kColDQ = (D == 64) ? 384 : 0;
+  static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
+  static constexpr bool kDQAliasesDP = (D != 64);
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 template <int D, bool CAUSAL>
@@ -88,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
-  const WaitCtl ctl{abort_flag, args.err};
+  const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 2u};
   // iteration -> (query head, query tile)
   auto iter_head = [&](int i) { return b * sh.Hq + hk * group + i / per_head; };
   auto iter_q0 = [&](int i) { return (qt_first + i % per_head) * kTile; };
@@ -103,17 +117,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bDPFull), 1);
-    mbar_init(bar(L::bSTFree), 4);
-    mbar_init(bar(L::bDPFree), 4);
-    mbar_init(bar(L::bPReady), 4);
-    mbar_init(bar(L::bDSReady), 4);
-    mbar_init(bar(L::bPDSFree), 1);
+    mbar_init(bar(L::bPReady), 8);
+    mbar_init(bar(L::bDSReady), 8);
     mbar_init(bar(L::bDQFull), 1);
-    mbar_init(bar(L::bDQFree), 4);
-    mbar_init(bar(L::bLse + 0), 128);
-    mbar_init(bar(L::bLse + 1), 128);
+    mbar_init(bar(L::bDQFree), 8);
+    mbar_init(bar(L::bLse + 0), 256);
+    mbar_init(bar(L::bLse + 1), 256);
     mbar_init(bar(L::bMMADone), 1);
     mbar_init(bar(L::bDrain), 1);
+    mbar_init(bar(L::bRegs), 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -124,245 +136,262 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-
-  if (*abort_flag == 0) {
-    if (warp == 0) {
-      // ---------------- TMA producer ----------------
-      if (lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmdO);
-        mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTileBytes);
-        for (int p = 0; p < D / 64; ++p) {
-          tma_load_3d(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, k0, bhk);
-          tma_load_3d(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
-        }
-        int issued = 0;
-        for (int i = 0; i < n_iter; ++i) {
-          const int s = i % L::kStages;
-          const uint32_t ph = (i / L::kStages) & 1;
-          if (!wait_thread(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
-          issued = i + 1;
-          const int bhq = iter_head(i);
-          const int q0 = iter_q0(i);
-          mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTileBytes);
+  // Register split per warpgroup: launched with 168 per thread (384 x 168 =
+  // 64512); warpgroup 0 drops to 72 and the compute warpgroups rise to 216
+  // (128 x 72 + 256 x 216 = 64512); all return to 168 before the teardown.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    if (*abort_flag == 0) {
+      if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+          tma_prefetch_desc(&tmQ);
+          tma_prefetch_desc(&tmK);
+          tma_prefetch_desc(&tmV);
+          tma_prefetch_desc(&tmdO);
+          mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTileBytes);
           for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                        bar(L::bQFull + s), p * 64, q0, bhq);
-            tma_load_3d(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
-                        bar(L::bQFull + s), p * 64, q0, bhq);
+            tma_load_3d(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, k0, bhk);
+            tma_load_3d(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
           }
+          int issued = 0;
+          for (int i = 0; i < n_iter; ++i) {
+            const int s = i % L::kStages;
+            const uint32_t ph = (i / L::kStages) & 1;
+            if (!wait_thread(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
+            issued = i + 1;
+            const int bhq = iter_head(i);
+            const int q0 = iter_q0(i);
+            mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTileBytes);
+            for (int p = 0; p < D / 64; ++p) {
+              tma_load_3d(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                          bar(L::bQFull + s), p * 64, q0, bhq);
+              tma_load_3d(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
+                          bar(L::bQFull + s), p * 64, q0, bhq);
+            }
+          }
+          wait_drain(bar(L::bKVFull), 0, ctl);
+          for (int i = issued > L::kStages ? issued - L::kStages : 0; i < issued; ++i)
+            wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, ctl);
         }
-        wait_drain(bar(L::bKVFull), 0, args.err);
-        for (int i = issued > L::kStages ? issued - L::kStages : 0; i < issued; ++i)
-          wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, args.err);
-      }
-    } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
-        constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t idKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
-        constexpr uint32_t idMM = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
-        const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
-                       tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
-        bool ok = wait_thread(bar(L::bKVFull), 0, ctl);
-        for (int i = 0; ok && i < n_iter; ++i) {
-          const int s = i % L::kStages;
-          const uint32_t ph = (i / L::kStages) & 1;
-          const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
-          const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
-          if (!(ok = wait_thread(bar(L::bQFull + s), ph, ctl))) break;
-          if (i > 0) {
-            if (!(ok = wait_thread(bar(L::bSTFree), (i - 1) & 1, ctl))) break;
-            if (D == 128 && !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
+      } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+          constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+          constexpr uint32_t idKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
+          constexpr uint32_t idMM = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
+          const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
+                         tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
+          bool ok = wait_thread(bar(L::bKVFull), 0, ctl);
+          for (int i = 0; ok && i < n_iter; ++i) {
+            const int s = i % L::kStages;
+            const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
+            const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
+            if (!(ok = wait_thread(bar(L::bQFull + s), (i / L::kStages) & 1, ctl))) break;
+            tc_fence_after();
+            // S^T = K Q^T. The previous dV product read P^T from these columns and
+            // was issued earlier, so in-order execution protects it.
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+              umma_bf16(tS, sdesc_sw128(sbase + L::kK + koff, 16, 1024),
+                        sdesc_sw128(sQ + koff, 16, 1024), idKK, kk > 0);
+            }
+            umma_commit(bar(L::bSFull));
+            // dP^T = V dO^T (over the previous dQ when they share columns).
+            if (L::kDQAliasesDP && i > 0 &&
+                !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl)))
+              break;
+            tc_fence_after();
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+              umma_bf16(tDP, sdesc_sw128(sbase + L::kV + koff, 16, 1024),
+                        sdesc_sw128(sDO + koff, 16, 1024), idKK, kk > 0);
+            }
+            umma_commit(bar(L::bDPFull));
+            // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
+            if (!(ok = wait_thread(bar(L::bPReady), i & 1, ctl))) break;
+            tc_fence_after();
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16_tmem_a(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
+                               idKM, (i > 0 || kk > 0) ? 1u : 0u);
+            // dK += dS^T Q : A = dS^T in TMEM; dQ = dS K : A = dS^T smem read MN-major.
+            if (!(ok = wait_thread(bar(L::bDSReady), i & 1, ctl))) break;
+            tc_fence_after();
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16_tmem_a(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
+                               idKM, (i > 0 || kk > 0) ? 1u : 0u);
+            if (!L::kDQAliasesDP && i > 0 &&
+                !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl)))
+              break;
+            tc_fence_after();
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16(tDQ, sdesc_sw128(sbase + L::kDS + kk * 2048, L::kPanelBytes, 1024),
+                        sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
+            // dQ done also means the dS^T buffer and this Q / dO stage are free.
+            umma_commit(bar(L::bDQFull));
+            umma_commit(bar(L::bQEmpty + s));
           }
-          tc_fence_after();
-          // S^T = K Q^T : A = K [keys x d] K-major, B = Q [queries x d] K-major.
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tS, sdesc_sw128(sbase + L::kK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
-                      idKK, kk > 0);
-          }
-          umma_commit(bar(L::bSFull));
-          if (i > 0 && !(ok = wait_thread(bar(L::bDPFree), (i - 1) & 1, ctl))) break;
-          tc_fence_after();
-          // dP^T = V dO^T
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tDP, sdesc_sw128(sbase + L::kV + koff, 16, 1024),
-                      sdesc_sw128(sDO + koff, 16, 1024), idKK, kk > 0);
-          }
-          umma_commit(bar(L::bDPFull));
-          // dV += P^T dO : A = P^T [keys x queries] K-major, B = dO viewed [d x queries] MN-major.
-          if (!(ok = wait_thread(bar(L::bPReady), i & 1, ctl))) break;
-          tc_fence_after();
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tDV, sdesc_sw128(sbase + L::kP + aoff, 16, 1024),
-                      sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024), idKM,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          // dK += dS^T Q ; dQ = dS K (A = dS^T buffer read MN-major, B = K MN-major).
-          if (!(ok = wait_thread(bar(L::bDSReady), i & 1, ctl))) break;
-          tc_fence_after();
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tDK, sdesc_sw128(sbase + L::kDS + aoff, 16, 1024),
-                      sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024), idKM,
-                      (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (D == 64 && i > 0 && !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
-          tc_fence_after();
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            umma_bf16(tDQ, sdesc_sw128(sbase + L::kDS + kk * 2048, L::kPanelBytes, 1024),
-                      sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
-          }
-          umma_commit(bar(L::bDQFull));
-          umma_commit(bar(L::bQEmpty + s));
-          umma_commit(bar(L::bPDSFree));
+          umma_commit(bar(L::bMMADone));
+          umma_commit(bar(L::bDrain));
+          wait_drain(bar(L::bDrain), 0, ctl);
         }
-        umma_commit(bar(L::bMMADone));
-        umma_commit(bar(L::bDrain));
-        wait_drain(bar(L::bDrain), 0, args.err);
       }
-    } else {
+    }
+    __syncwarp();
+    // Reclaim registers only after both compute warpgroups have taken theirs:
+    // otherwise an early exit of this group could take the registers they are
+    // waiting for. Their arrival follows their first instruction, so this wait is
+    // short; it is bounded like every other wait.
+    wait_drain(bar(L::bRegs), 0, ctl);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bRegs));
+    if (*abort_flag == 0) {
       // ---------------- compute warps ----------------
       const uint32_t quarter = warp & 3;
-      const int r = quarter * 32 + lane;  // TMEM lane: key row for S^T/dP^T, query row for dQ
-      const int ct = threadIdx.x - 64;    // 0..127
+      const int half = (warp - 4) >> 2;          // query columns [64 half, 64 half + 64)
+      const int r = quarter * 32 + lane;         // TMEM lane: key row (S^T, dP^T) / query row (dQ)
+      const int ct = threadIdx.x - 128;          // 0..255
       const uint32_t lane_off = (quarter * 32u) << 16;
       const int key = k0 + r;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
-      const float* lse_s = reinterpret_cast<const float*>(smem + L::kLse);
-      const float* dl_s = reinterpret_cast<const float*>(smem + L::kDelta);
+      float* lse_s = reinterpret_cast<float*>(smem + L::kLse);
+      float* dl_s = reinterpret_cast<float*>(smem + L::kDelta);
+      constexpr int kDH = D / 2;                 // dQ / dK / dV columns per warp
       bool ok = true;
+
+      // dQ of iteration `it` from TMEM (this thread: query row q0 + r, columns
+      // [kDH half, kDH half + kDH)) -> alpha dQ reduce-added into the workspace.
+      auto drain_dq = [&](int it) -> bool {
+        if (!wait_warp(bar(L::bDQFull), it & 1, ctl)) return false;
+        tc_fence_after();
+        const int q = iter_q0(it) + r;
+        float* dq_row = args.dq_accum + (static_cast<size_t>(iter_head(it)) * N + q) * D + kDH * half;
+#pragma unroll
+        for (int c = 0; c < kDH; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half + c, v);
+          tmem_ld_wait32(v);
+          if (q < N) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              atomicAdd(reinterpret_cast<float4*>(dq_row + c) + u,
+                        make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
+                                    alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bDQFree));
+        return true;
+      };
 
       for (int i = 0; ok && i < n_iter; ++i) {
         const int bhq = iter_head(i);
         const int q0 = iter_q0(i);
         const int slot = i & 1;
         {
-          const int q = q0 + ct;
-          float* lw = reinterpret_cast<float*>(smem + L::kLse) + slot * kTile;
-          float* dw = reinterpret_cast<float*>(smem + L::kDelta) + slot * kTile;
-          lw[ct] = (q < N) ? args.lse[static_cast<size_t>(bhq) * N + q] * kLog2e : INFINITY;
-          dw[ct] = (q < N) ? args.delta[static_cast<size_t>(bhq) * N + q] : 0.f;
+          const int c = ct & (kTile - 1);
+          const int q = q0 + c;
+          if (ct < kTile)
+            lse_s[slot * kTile + c] = (q < N) ? args.lse[static_cast<size_t>(bhq) * N + q] * kLog2e : INFINITY;
+          else
+            dl_s[slot * kTile + c] = (q < N) ? args.delta[static_cast<size_t>(bhq) * N + q] : 0.f;
         }
-        // All 128 compute threads have staged their value (and, by the previous
-        // iteration's wait, finished reading this slot two iterations ago).
+        // All 256 compute threads have staged their value (and, through the
+        // previous iteration's wait, finished reading this slot two iterations ago).
         mbar_arrive(bar(L::bLse + slot));
         if (!(ok = wait_warp(bar(L::bLse + slot), (i >> 1) & 1, ctl))) break;
-        const float* lrow = lse_s + slot * kTile;
-        const float* drow = dl_s + slot * kTile;
-        const bool need_mask = (CAUSAL && q0 == k0) || (k0 + kTile > N);
 
-        // P^T row: p[c] = exp(alpha s - lse_c), query c visible to this key.
+        // The previous tile's dQ (overlaps this tile's S^T product).
+        if (i > 0 && !(ok = drain_dq(i - 1))) break;
+
+        // P^T = exp(alpha S^T - lse) for this thread's 64 queries.
+        const bool diag = CAUSAL && q0 == k0;
         if (!(ok = wait_warp(bar(L::bSFull), i & 1, ctl))) break;
         tc_fence_after();
-        float p[kTile];
+        uint32_t sv[64];
+        tmem_ld64(tmem + L::kColS + lane_off + 64 * half, sv);
+        tmem_ld_wait64(sv);
+        float p[64];
+        const float4* l4 = reinterpret_cast<const float4*>(lse_s + slot * kTile + 64 * half);
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(tmem + L::kColS + lane_off + c4 * 32, v);
-          tmem_ld_wait32(v);
-#pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const int c = c4 * 32 + t;
-            float pv = ex2_approx(fmaf(__uint_as_float(v[t]), sl2, -lrow[c]));
-            if (need_mask) {
-              const bool vis = key < N && (!CAUSAL || q0 + c >= key);
-              pv = vis ? pv : 0.f;
-            }
-            p[c] = pv;
-          }
+        for (int u = 0; u < 16; ++u) {
+          const float4 lq = l4[u];
+          fma2v(p[4 * u], p[4 * u + 1], __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]),
+                sl2, sl2, -lq.x, -lq.y);
+          fma2v(p[4 * u + 2], p[4 * u + 3], __uint_as_float(sv[4 * u + 2]),
+                __uint_as_float(sv[4 * u + 3]), sl2, sl2, -lq.z, -lq.w);
         }
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = ex2_approx(p[c]);
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (q0 + 64 * half + c < key) p[c] = 0.f;
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
+          tmem_st32(tmem + L::kColS + lane_off + 64 * half, pk);
+        }
+        tmem_st_wait();
         tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bSTFree));
-
-        if (i > 0 && !(ok = wait_warp(bar(L::bPDSFree), (i - 1) & 1, ctl))) break;
-        // P^T (BF16) into the swizzled [keys][queries] buffer.
-#pragma unroll
-        for (int c8 = 0; c8 < kTile / 8; ++c8) {
-          const uint32_t addr = sbase + L::kP + (c8 >> 3) * L::kPanelBytes + sw128_offset(r, c8 & 7);
-          st_shared_v4(addr, pack_bf16x2(p[8 * c8 + 0], p[8 * c8 + 1]),
-                       pack_bf16x2(p[8 * c8 + 2], p[8 * c8 + 3]),
-                       pack_bf16x2(p[8 * c8 + 4], p[8 * c8 + 5]),
-                       pack_bf16x2(p[8 * c8 + 6], p[8 * c8 + 7]));
-        }
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPReady));
 
-        // dS^T = alpha P^T o (dP^T - delta)
+        // dS^T = P^T o (dP^T - delta) (alpha is applied to dK and dQ at the end).
         if (!(ok = wait_warp(bar(L::bDPFull), i & 1, ctl))) break;
         tc_fence_after();
+        tmem_ld64(tmem + L::kColDP + lane_off + 64 * half, sv);
+        tmem_ld_wait64(sv);
+        const float4* d4 = reinterpret_cast<const float4*>(dl_s + slot * kTile + 64 * half);
+        uint32_t pk[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t v[32];
-          tmem_ld32(tmem + L::kColDP + lane_off + c4 * 32, v);
-          tmem_ld_wait32(v);
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = c4 * 32 + c8 * 8 + 2 * u;
-              const float d0 = alpha * p[c] * (__uint_as_float(v[c8 * 8 + 2 * u]) - drow[c]);
-              const float d1 =
-                  alpha * p[c + 1] * (__uint_as_float(v[c8 * 8 + 2 * u + 1]) - drow[c + 1]);
-              w[u] = pack_bf16x2(d0, d1);
-            }
-            const int chunk = c4 * 4 + c8;  // 16-byte chunk index over 128 queries
-            const uint32_t addr =
-                sbase + L::kDS + (chunk >> 3) * L::kPanelBytes + sw128_offset(r, chunk & 7);
-            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
-          }
+        for (int u = 0; u < 16; ++u) {
+          const float4 dq = d4[u];
+          float t0, t1, t2, t3;
+          fma2v(t0, t1, __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]), 1.f, 1.f, -dq.x, -dq.y);
+          fma2v(t2, t3, __uint_as_float(sv[4 * u + 2]), __uint_as_float(sv[4 * u + 3]), 1.f, 1.f, -dq.z, -dq.w);
+          mul2v(t0, t1, t0, t1, p[4 * u], p[4 * u + 1]);
+          mul2v(t2, t3, t2, t3, p[4 * u + 2], p[4 * u + 3]);
+          pk[2 * u] = pack_bf16x2(t0, t1);
+          pk[2 * u + 1] = pack_bf16x2(t2, t3);
         }
-        tc_fence_before();
+        tmem_st32(tmem + L::kColDP + lane_off + 64 * half, pk);
+        // dS^T row into the swizzled [keys][queries] buffer, panel `half`. The
+        // previous dQ product (its reader) completed before drain_dq returned.
+        {
+          const uint32_t rowb = sbase + L::kDS + half * L::kPanelBytes;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(rowb + sw128_offset(r, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(L::bDPFree));
-          mbar_arrive(bar(L::bDSReady));
-        }
-
-        // dQ tile -> FP32 reduce-add into the workspace (this thread = query row q0 + r).
-        if (!(ok = wait_warp(bar(L::bDQFull), i & 1, ctl))) break;
-        tc_fence_after();
-        const int q = q0 + r;
-        float* dq_row = args.dq_accum + (static_cast<size_t>(bhq) * N + q) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + L::kColDQ + lane_off + c, v);
-          tmem_ld_wait32(v);
-          if (q < N) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              atomicAdd(reinterpret_cast<float4*>(dq_row + c) + u,
-                        make_float4(__uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                                    __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3])));
-          }
-        }
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bDQFree));
+        if (lane == 0) mbar_arrive(bar(L::bDSReady));
       }
+      if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
 
-      // ---------------- epilogue: dK, dV rows of this key tile ----------------
+      // ---------------- epilogue: dK (x alpha), dV rows of this key tile ----------------
       if (ok) ok = wait_warp(bar(L::bMMADone), 0, ctl);
       if (ok) {
         tc_fence_after();
         const size_t row = static_cast<size_t>(bhk) * N + key;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
-          const uint32_t col = which == 0 ? L::kColDK : L::kColDV;
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(which == 0 ? args.dk : args.dv) + row * D;
+          const uint32_t col = (which == 0 ? L::kColDK : L::kColDV) + kDH * half;
+          const float sc = which == 0 ? alpha : 1.f;
+          __nv_bfloat16* out =
+              reinterpret_cast<__nv_bfloat16*>(which == 0 ? args.dk : args.dv) + row * D + kDH * half;
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
+          for (int c = 0; c < kDH; c += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + col + lane_off + c, v);
             tmem_ld_wait32(v);
@@ -370,15 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
               for (int u = 0; u < 4; ++u)
-                dst[u] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1])),
-                                    pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3])),
-                                    pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5])),
-                                    pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7])));
+                dst[u] = make_uint4(pack_bf16x2(sc * __uint_as_float(v[8 * u + 0]), sc * __uint_as_float(v[8 * u + 1])),
+                                    pack_bf16x2(sc * __uint_as_float(v[8 * u + 2]), sc * __uint_as_float(v[8 * u + 3])),
+                                    pack_bf16x2(sc * __uint_as_float(v[8 * u + 4]), sc * __uint_as_float(v[8 * u + 5])),
+                                    pack_bf16x2(sc * __uint_as_float(v[8 * u + 6]), sc * __uint_as_float(v[8 * u + 7])));
             }
           }
         }
       }
     }
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
   }
 
   tc_fence_before();

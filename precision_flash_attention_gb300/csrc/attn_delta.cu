@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
-  const WaitCtl ctl{abort_flag, args.err};
+  const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 3u};
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
@@ -143,9 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
           }
         }
-        wait_drain(bar(L::bQFull), 0, args.err);
+        wait_drain(bar(L::bQFull), 0, ctl);
         for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
-          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, args.err);
+          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(bar(L::bKVEmpty + s));
         }
         umma_commit(bar(L::bDrain));
-        wait_drain(bar(L::bDrain), 0, args.err);
+        wait_drain(bar(L::bDrain), 0, ctl);
       }
     } else {
       const uint32_t quarter = warp & 3;

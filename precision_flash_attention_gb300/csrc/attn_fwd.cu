@@ -48,7 +48,8 @@ struct FwdLayout {
   static constexpr int bPFull = bSFull + 2;           // + tile
   static constexpr int bODone = bPFull + 2;           // + tile
   static constexpr int bDrain = bODone + 2;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bRegs = bDrain + 1;          // the softmax warps hold their registers
+  static constexpr int kNumBars = bRegs + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
-  const WaitCtl ctl{abort_flag, args.err};
+  const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 1u};
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
@@ -103,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bODone + t), 1);
     }
     mbar_init(bar(L::bDrain), 1);
+    mbar_init(bar(L::bRegs), 8);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -146,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // Drain: every issued copy has landed before shared memory is released.
-        wait_drain(bar(L::bQFull), 0, args.err);
+        wait_drain(bar(L::bQFull), 0, ctl);
         for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
-          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, args.err);
+          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
       }
     } else if (warp == 1) {
       // ---------------- MMA issuer ----------------
@@ -206,14 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Drain: no MMA may still read shared memory or write TMEM at teardown.
         umma_commit(bar(L::bDrain));
-        wait_drain(bar(L::bDrain), 0, args.err);
+        wait_drain(bar(L::bDrain), 0, ctl);
       }
     }
     }
     __syncwarp();
+    // Reclaim registers only after both compute warpgroups have taken theirs:
+    // otherwise an early exit of this group could take the registers they are
+    // waiting for. Their arrival follows their first instruction, so this wait is
+    // short; it is bounded like every other wait.
+    wait_drain(bar(L::bRegs), 0, ctl);
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bRegs));
     if (*abort_flag == 0) {
       // ---------------- softmax warps ----------------
       const int t = (warp - 4) >> 2;  // query tile of this warpgroup

@@ -55,6 +55,22 @@ __device__ __forceinline__ void fma2(float& y0, float& y1, float x0, float x1, f
       : "=f"(y0), "=f"(y1)
       : "f"(x0), "f"(x1), "f"(a), "f"(b));
 }
+// y = x * a + b lane-wise, with per-lane a and b.
+__device__ __forceinline__ void fma2v(float& y0, float& y1, float x0, float x1, float a0, float a1,
+                                      float b0, float b1) {
+  asm("{\n\t.reg .b64 xa, aa, ba, ya;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 aa, {%4, %5};\n\tmov.b64 ba, {%6, %7};\n\t"
+      "fma.rn.f32x2 ya, xa, aa, ba;\n\tmov.b64 {%0, %1}, ya;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2v(float& y0, float& y1, float x0, float x1, float a0, float a1) {
+  asm("{\n\t.reg .b64 xa, aa, ya;\n\t"
+      "mov.b64 xa, {%2, %3};\n\tmov.b64 aa, {%4, %5};\n\t"
+      "mul.rn.f32x2 ya, xa, aa;\n\tmov.b64 {%0, %1}, ya;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a0), "f"(a1));
+}
 __device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
   asm("{\n\t.reg .b64 sa, xa;\n\t"
       "mov.b64 sa, {%0, %1};\n\tmov.b64 xa, {%2, %3};\n\t"
@@ -121,19 +137,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Per-CTA control block for bounded waits. `abort` lives in shared memory; once
 // any thread gives up on a wait it is set and every other wait returns false
-// promptly, so all roles reach the common teardown.
+// promptly, so all roles reach the common teardown. The first wait to give up
+// in a launch also records where: kernel id, barrier offset, parity and block.
 struct WaitCtl {
-  volatile int* abort;  // shared memory
-  int* err;             // global error word (may be null)
+  volatile int* abort;           // shared memory
+  int* err;                      // global error word (may be null)
+  unsigned long long* site;      // global error-site word (may be null)
+  uint32_t smem_base;            // shared address of the CTA's dynamic shared memory
+  uint32_t kernel;               // 1 forward, 2 backward, 3 delta via dP o P
 };
 
 // Wait budget per wait: a correct pipeline waits micro-seconds; a stuck one
 // is abandoned after about a second.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
-__device__ __forceinline__ void raise_error(const WaitCtl& c, int code) {
+// Error site encoding: bit 63 set, kernel in bits 56-59, bit 55 drain wait,
+// bit 54 parity, barrier byte offset in bits 32-53, blockIdx.x in bits 0-31.
+__device__ __forceinline__ void raise_error(const WaitCtl& c, int code, uint32_t bar, uint32_t parity,
+                                            bool drain) {
   *c.abort = 1;
   if (c.err) atomicOr(c.err, code);
+  if (c.site) {
+    const unsigned long long w = (1ull << 63) | (static_cast<unsigned long long>(c.kernel & 15u) << 56) |
+                                 (static_cast<unsigned long long>(drain ? 1u : 0u) << 55) |
+                                 (static_cast<unsigned long long>(parity & 1u) << 54) |
+                                 (static_cast<unsigned long long>((bar - c.smem_base) & 0x3FFFFFu) << 32) |
+                                 static_cast<unsigned long long>(blockIdx.x);
+    atomicCAS(c.site, 0ull, w);
+  }
 }
 
 // Single-thread wait (producer / MMA issuer). Returns false on timeout/abort.
@@ -145,7 +176,7 @@ __device__ __forceinline__ bool wait_thread(uint32_t bar, uint32_t parity, const
     if ((it & 15u) == 0) {
       if (*c.abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
-        raise_error(c, PFA_DEVERR_TIMEOUT);
+        raise_error(c, PFA_DEVERR_TIMEOUT, bar, parity, false);
         return false;
       }
     }
@@ -165,7 +196,7 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const W
         if (*c.abort) {
           give_up = 1;
         } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-          raise_error(c, PFA_DEVERR_TIMEOUT);
+          raise_error(c, PFA_DEVERR_TIMEOUT, bar, parity, false);
           give_up = 1;
         }
       }
@@ -176,11 +207,11 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const W
 
 // Teardown wait that ignores the abort flag: used to let in-flight TMA copies
 // and MMAs finish before the CTA releases its shared memory and TMEM.
-__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) {
-      if (err) atomicOr(err, PFA_DEVERR_TIMEOUT);
+      raise_error(c, PFA_DEVERR_TIMEOUT, bar, parity, true);
       return false;
     }
   }

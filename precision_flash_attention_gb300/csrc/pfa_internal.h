@@ -25,6 +25,7 @@ struct FwdArgs {
   float* lse;              // [B, Hq, N]
   long long* counters;     // 3 x int64 or null
   int* err;                // device error word
+  unsigned long long* err_site;  // where the first bounded wait gave up
   int fix_mode;
   float beta;
   float eps_raw;           // tie tolerance in units of the unscaled score Q.K
@@ -36,6 +37,7 @@ struct DeltaAltArgs {
   const float* lse;
   float* delta;
   int* err;
+  unsigned long long* err_site;
 };
 
 struct BwdArgs {
@@ -46,6 +48,7 @@ struct BwdArgs {
   void* dk;                // bf16 [B, Hkv, N, d]
   void* dv;                // bf16 [B, Hkv, N, d]
   int* err;
+  unsigned long long* err_site;
 };
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
