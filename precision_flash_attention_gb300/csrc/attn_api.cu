@@ -96,6 +96,22 @@ int tile_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? PFA_OK : PFA_ERR_INVALID_ARG;
 }
 
+// [B*H, N, d] FP32 tensor (the dQ workspace), boxes of 32 columns (128 bytes,
+// 128B swizzle) x 32 rows: one compute warp's share of a dQ tile.
+int f32_box_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PFA_OK : PFA_ERR_INVALID_ARG;
+}
+
 pfa::AttnShape shape(int B, int Hq, int Hkv, int N, int d, int causal, float scale) {
   pfa::AttnShape s;
   s.B = B;
@@ -218,6 +234,8 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
+  CUtensorMap tdq;
+  if ((rc = f32_box_map(&tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
   if ((rc = launched(cudaMemsetAsync(dq_accum, 0, ws, st))) != PFA_OK) return rc;
@@ -230,7 +248,7 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   a.dv = dv;
   a.err = dev->err;
   a.err_site = dev->site;
-  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, a, st))) != PFA_OK) return rc;
+  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, tdq, a, st))) != PFA_OK) return rc;
   return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
 }
 

@@ -23,6 +23,10 @@
 // Tensor-core order per query tile: S^T, dP^T, dV, dK, dQ; the P phase of the
 // compute warps overlaps dP^T and the dS phase overlaps dV.
 #include "pfa_device.cuh"
+#include "pfa_trace.cuh"
+
+PFA_TRACE_BUFFER(g_pfa_bwd_trace);
+#define PFA_BWD_TRACE(slot, ev, j) PFA_TRACE_EVENT(g_pfa_bwd_trace, slot, ev, j)
 
 namespace pfa {
 namespace {
@@ -40,17 +44,23 @@ __host__ __device__ constexpr uint32_t packed_col(int kk) {
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kStages = 2;
+  // Query-side stages: the next tile's Q / dO must land within about one
+  // iteration, so d = 64 keeps three in flight; d = 128 fits two.
+  static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kPanelBytes = kTile * 128;
+  // dQ leaves through a TMA reduce-add from a per-warp staging box (d = 64:
+  // 32 rows x 32 FP32 columns, 4 KB per compute warp); d = 128 has no room left
+  // for the staging and reduce-adds with vector atomics.
+  static constexpr bool kTmaDQ = (D == 64);
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;                // + stage * tile
   static constexpr int kDO = kQ + kStages * kTileBytes;     // + stage * tile
   static constexpr int kDS = kDO + kStages * kTileBytes;    // dS^T [keys][queries] bf16, 2 panels
-  static constexpr int kLse = kDS + kTile * kTile * 2;      // 2 slots x 128 floats (x log2 e)
-  static constexpr int kDelta = kLse + 2 * kTile * 4;       // 2 slots x 128 floats
-  static constexpr int kBars = kDelta + 2 * kTile * 4;
+  static constexpr int kDQStage = kDS + kTile * kTile * 2;  // 8 warps x 4 KB (d = 64 only)
+  static constexpr int kLse = kDQStage + (kTmaDQ ? 8 * 4096 : 0);  // [slot 2][half 2][lse 64 | delta 64]
+  static constexpr int kBars = kLse + 2 * 2 * 128 * 4;
   static constexpr int bKVFull = 0;
   static constexpr int bQFull = 1;                  // + stage
   static constexpr int bQEmpty = bQFull + kStages;  // + stage
@@ -60,8 +70,8 @@ struct BwdLayout {
   static constexpr int bDSReady = bPReady + 1;
   static constexpr int bDQFull = bDSReady + 1;
   static constexpr int bDQFree = bDQFull + 1;
-  static constexpr int bLse = bDQFree + 1;          // + slot (2)
-  static constexpr int bMMADone = bLse + 2;
+  static constexpr int bLse = bDQFree + 1;          // + 2 * half + slot
+  static constexpr int bMMADone = bLse + 4;
   static constexpr int bDrain = bMMADone + 1;
   static constexpr int bRegs = bDrain + 1;          // the compute warps hold their registers
   static constexpr int kNumBars = bRegs + 1;
@@ -71,6 +81,7 @@ struct BwdLayout {
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
   static constexpr bool kDQAliasesDP = (D != 64);
+  static_assert(kDQStage % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -78,12 +89,13 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdArgs args) {
+                    const __grid_constant__ CUtensorMap tmdQ, const BwdArgs args) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  PFA_TRACE_DECL();
 
   const AttnShape& sh = args.s;
   const int N = sh.N;
@@ -121,8 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::bDSReady), 8);
     mbar_init(bar(L::bDQFull), 1);
     mbar_init(bar(L::bDQFree), 8);
-    mbar_init(bar(L::bLse + 0), 256);
-    mbar_init(bar(L::bLse + 1), 256);
+    for (int x = 0; x < 4; ++x) mbar_init(bar(L::bLse + x), 4);
     mbar_init(bar(L::bMMADone), 1);
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bRegs), 8);
@@ -143,98 +154,120 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
     if (*abort_flag == 0) {
       if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        if (lane == 0) {
-          tma_prefetch_desc(&tmQ);
-          tma_prefetch_desc(&tmK);
-          tma_prefetch_desc(&tmV);
-          tma_prefetch_desc(&tmdO);
-          mbar_arrive_expect_tx(bar(L::bKVFull), 2 * L::kTileBytes);
+        // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+        tma_prefetch_desc_warp(&tmQ);
+        tma_prefetch_desc_warp(&tmK);
+        tma_prefetch_desc_warp(&tmV);
+        tma_prefetch_desc_warp(&tmdO);
+        if (L::kTmaDQ) tma_prefetch_desc_warp(&tmdQ);
+        mbar_arrive_expect_tx_warp(bar(L::bKVFull), 2 * L::kTileBytes);
+        for (int p = 0; p < D / 64; ++p) {
+          tma_load_3d_warp(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, k0, bhk);
+          tma_load_3d_warp(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
+        }
+        int issued = 0;
+        for (int i = 0; i < n_iter; ++i) {
+          const int s = i % L::kStages;
+          const uint32_t ph = (i / L::kStages) & 1;
+          if (!wait_warp(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
+          issued = i + 1;
+          const int bhq = iter_head(i);
+          const int q0 = iter_q0(i);
+          mbar_arrive_expect_tx_warp(bar(L::bQFull + s), 2 * L::kTileBytes);
           for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, k0, bhk);
-            tma_load_3d(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
+            tma_load_3d_warp(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                             bar(L::bQFull + s), p * 64, q0, bhq);
+            tma_load_3d_warp(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
+                             bar(L::bQFull + s), p * 64, q0, bhq);
           }
-          int issued = 0;
-          for (int i = 0; i < n_iter; ++i) {
-            const int s = i % L::kStages;
-            const uint32_t ph = (i / L::kStages) & 1;
-            if (!wait_thread(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
-            issued = i + 1;
-            const int bhq = iter_head(i);
-            const int q0 = iter_q0(i);
-            mbar_arrive_expect_tx(bar(L::bQFull + s), 2 * L::kTileBytes);
-            for (int p = 0; p < D / 64; ++p) {
-              tma_load_3d(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                          bar(L::bQFull + s), p * 64, q0, bhq);
-              tma_load_3d(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
-                          bar(L::bQFull + s), p * 64, q0, bhq);
-            }
-          }
-          wait_drain(bar(L::bKVFull), 0, ctl);
-          for (int i = issued > L::kStages ? issued - L::kStages : 0; i < issued; ++i)
-            wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, ctl);
         }
+        wait_drain(bar(L::bKVFull), 0, ctl);
+        for (int i = issued > L::kStages ? issued - L::kStages : 0; i < issued; ++i)
+          wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, ctl);
       } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-          constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
-          constexpr uint32_t idKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
-          constexpr uint32_t idMM = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
-          const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
-                         tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
-          bool ok = wait_thread(bar(L::bKVFull), 0, ctl);
-          for (int i = 0; ok && i < n_iter; ++i) {
-            const int s = i % L::kStages;
-            const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
-            const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
-            if (!(ok = wait_thread(bar(L::bQFull + s), (i / L::kStages) & 1, ctl))) break;
-            tc_fence_after();
-            // S^T = K Q^T. The previous dV product read P^T from these columns and
-            // was issued earlier, so in-order execution protects it.
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-              umma_bf16(tS, sdesc_sw128(sbase + L::kK + koff, 16, 1024),
-                        sdesc_sw128(sQ + koff, 16, 1024), idKK, kk > 0);
-            }
-            umma_commit(bar(L::bSFull));
-            // dP^T = V dO^T (over the previous dQ when they share columns).
-            if (L::kDQAliasesDP && i > 0 &&
-                !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl)))
-              break;
-            tc_fence_after();
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-              umma_bf16(tDP, sdesc_sw128(sbase + L::kV + koff, 16, 1024),
-                        sdesc_sw128(sDO + koff, 16, 1024), idKK, kk > 0);
-            }
-            umma_commit(bar(L::bDPFull));
-            // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
-            if (!(ok = wait_thread(bar(L::bPReady), i & 1, ctl))) break;
-            tc_fence_after();
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_bf16_tmem_a(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
-                               idKM, (i > 0 || kk > 0) ? 1u : 0u);
-            // dK += dS^T Q : A = dS^T in TMEM; dQ = dS K : A = dS^T smem read MN-major.
-            if (!(ok = wait_thread(bar(L::bDSReady), i & 1, ctl))) break;
-            tc_fence_after();
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_bf16_tmem_a(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
-                               idKM, (i > 0 || kk > 0) ? 1u : 0u);
-            if (!L::kDQAliasesDP && i > 0 &&
-                !(ok = wait_thread(bar(L::bDQFree), (i - 1) & 1, ctl)))
-              break;
-            tc_fence_after();
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              umma_bf16(tDQ, sdesc_sw128(sbase + L::kDS + kk * 2048, L::kPanelBytes, 1024),
-                        sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
-            // dQ done also means the dS^T buffer and this Q / dO stage are free.
-            umma_commit(bar(L::bDQFull));
-            umma_commit(bar(L::bQEmpty + s));
+        // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+        // Order per query tile i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1). S^T(i+1)
+        // overwrites P^T(i) after dV(i) has read it and runs while the compute warps
+        // form dS(i); dP^T(i+1) overwrites dS^T(i) after dK(i) has read it.
+        constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+        constexpr uint32_t idKM = idesc_bf16(128, D, false, true);     // dV, dK: B MN-major
+        constexpr uint32_t idMM = idesc_bf16(128, D, true, true);      // dQ: A and B MN-major
+        const uint32_t tS = tmem + L::kColS, tDP = tmem + L::kColDP, tDV = tmem + L::kColDV,
+                       tDK = tmem + L::kColDK, tDQ = tmem + L::kColDQ;
+        // S^T = K Q^T and dP^T = V dO^T of query tile i.
+        auto issue_s = [&](int i) {
+          const uint32_t sQ = sbase + L::kQ + (i % L::kStages) * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+            umma_bf16_warp(tS, sdesc_sw128(sbase + L::kK + koff, 16, 1024),
+                           sdesc_sw128(sQ + koff, 16, 1024), idKK, kk > 0);
           }
-          umma_commit(bar(L::bMMADone));
-          umma_commit(bar(L::bDrain));
-          wait_drain(bar(L::bDrain), 0, ctl);
+          umma_commit_warp(bar(L::bSFull));
+        };
+        auto issue_dp = [&](int i) {
+          const uint32_t sDO = sbase + L::kDO + (i % L::kStages) * L::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+            umma_bf16_warp(tDP, sdesc_sw128(sbase + L::kV + koff, 16, 1024),
+                           sdesc_sw128(sDO + koff, 16, 1024), idKK, kk > 0);
+          }
+          umma_commit_warp(bar(L::bDPFull));
+        };
+        bool ok = wait_warp(bar(L::bKVFull), 0, ctl);
+        if (ok && n_iter > 0 && (ok = wait_warp(bar(L::bQFull), 0, ctl))) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
         }
+        for (int i = 0; ok && i < n_iter; ++i) {
+          const int s = i % L::kStages;
+          const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
+          const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
+          const bool more = i + 1 < n_iter;
+          // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
+          if (!(ok = wait_warp(bar(L::bPReady), i & 1, ctl))) break;
+          if (lane == 0) PFA_BWD_TRACE(0, 2, i);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_tmem_a_warp(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
+                                  idKM, (i > 0 || kk > 0) ? 1u : 0u);
+          if (more) {
+            const int s1 = (i + 1) % L::kStages;
+            if (!(ok = wait_warp(bar(L::bQFull + s1), ((i + 1) / L::kStages) & 1, ctl))) break;
+            if (lane == 0) PFA_BWD_TRACE(0, 1, i + 1);
+            tc_fence_after();
+            issue_s(i + 1);
+          }
+          // dK += dS^T Q : A = dS^T in TMEM; dQ = dS K : A = dS^T smem read MN-major.
+          if (!(ok = wait_warp(bar(L::bDSReady), i & 1, ctl))) break;
+          if (lane == 0) PFA_BWD_TRACE(0, 3, i);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_tmem_a_warp(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
+                                  idKM, (i > 0 || kk > 0) ? 1u : 0u);
+          if (!L::kDQAliasesDP && i > 0 && !(ok = wait_warp(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            umma_bf16_warp(tDQ, sdesc_sw128(sbase + L::kDS + kk * 2048, L::kPanelBytes, 1024),
+                           sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
+          // dQ done also means the dS^T buffer and this Q / dO stage are free.
+          umma_commit_warp(bar(L::bDQFull));
+          umma_commit_warp(bar(L::bQEmpty + s));
+          if (more) {
+            // With dQ over the dP^T columns, dP^T(i+1) waits until dQ(i) is drained.
+            if (L::kDQAliasesDP && !(ok = wait_warp(bar(L::bDQFree), i & 1, ctl))) break;
+            tc_fence_after();
+            issue_dp(i + 1);
+          }
+        }
+        umma_commit_warp(bar(L::bMMADone));
+        umma_commit_warp(bar(L::bDrain));
+        wait_drain(bar(L::bDrain), 0, ctl);
       }
     }
     __syncwarp();
@@ -253,71 +286,109 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t quarter = warp & 3;
       const int half = (warp - 4) >> 2;          // query columns [64 half, 64 half + 64)
       const int r = quarter * 32 + lane;         // TMEM lane: key row (S^T, dP^T) / query row (dQ)
-      const int ct = threadIdx.x - 128;          // 0..255
       const uint32_t lane_off = (quarter * 32u) << 16;
       const int key = k0 + r;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
-      float* lse_s = reinterpret_cast<float*>(smem + L::kLse);
-      float* dl_s = reinterpret_cast<float*>(smem + L::kDelta);
       constexpr int kDH = D / 2;                 // dQ / dK / dV columns per warp
+      const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 4) * 4096u;
       bool ok = true;
+
+      // Per-half staging of lse (x log2 e) and delta: slot [slot][half] holds the
+      // half's 64 lse values then its 64 deltas. Thread r of the half stages entry
+      // r; the value is loaded one iteration ahead so the load latency overlaps
+      // the previous tile.
+      auto stage_src = [&](int it) -> const float* {
+        const int q = iter_q0(it) + 64 * half + (r & 63);
+        if (q >= N) return nullptr;
+        const size_t off = static_cast<size_t>(iter_head(it)) * N + q;
+        return r < 64 ? args.lse + off : args.delta + off;
+      };
+      float pre = 0.f;
+      bool pre_in = false;
+      if (n_iter > 0) {
+        const float* src = stage_src(0);
+        pre_in = src != nullptr;
+        if (pre_in) pre = __ldg(src);
+      }
 
       // dQ of iteration `it` from TMEM (this thread: query row q0 + r, columns
       // [kDH half, kDH half + kDH)) -> alpha dQ reduce-added into the workspace.
       auto drain_dq = [&](int it) -> bool {
         if (!wait_warp(bar(L::bDQFull), it & 1, ctl)) return false;
         tc_fence_after();
-        const int q = iter_q0(it) + r;
-        float* dq_row = args.dq_accum + (static_cast<size_t>(iter_head(it)) * N + q) * D + kDH * half;
-#pragma unroll
-        for (int c = 0; c < kDH; c += 32) {
+        if constexpr (L::kTmaDQ) {
           uint32_t v[32];
-          tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half + c, v);
+          tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half, v);
           tmem_ld_wait32(v);
-          if (q < N) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::bDQFree));
+          // This warp's previous box has been read out of the staging buffer.
+          bulk_wait_read_warp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              atomicAdd(reinterpret_cast<float4*>(dq_row + c) + u,
-                        make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
-                                    alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
+          for (int c = 0; c < 8; ++c)
+            st_shared_v4(dq_stage + sw128_offset(lane, c),
+                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 0])),
+                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 1])),
+                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 2])),
+                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 3])));
+          fence_proxy_async_smem();
+          __syncwarp();
+          tma_reduce_add_3d_warp(&tmdQ, dq_stage, kDH * half, iter_q0(it) + 32 * static_cast<int>(quarter),
+                                 iter_head(it));
+        } else {
+          const int q = iter_q0(it) + r;
+          float* dq_row = args.dq_accum + (static_cast<size_t>(iter_head(it)) * N + q) * D + kDH * half;
+#pragma unroll
+          for (int c = 0; c < kDH; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half + c, v);
+            tmem_ld_wait32(v);
+            if (q < N) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                atomicAdd(reinterpret_cast<float4*>(dq_row + c) + u,
+                          make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
+                                      alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
+            }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::bDQFree));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bDQFree));
         return true;
       };
 
       for (int i = 0; ok && i < n_iter; ++i) {
-        const int bhq = iter_head(i);
         const int q0 = iter_q0(i);
         const int slot = i & 1;
-        {
-          const int c = ct & (kTile - 1);
-          const int q = q0 + c;
-          if (ct < kTile)
-            lse_s[slot * kTile + c] = (q < N) ? args.lse[static_cast<size_t>(bhq) * N + q] * kLog2e : INFINITY;
-          else
-            dl_s[slot * kTile + c] = (q < N) ? args.delta[static_cast<size_t>(bhq) * N + q] : 0.f;
+        float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 2 + half) * 128;
+        // Entry r of this slot was last read two tiles ago; every warp of the half
+        // has passed the previous tile's wait since, so no one still reads it.
+        stage[r] = r < 64 ? (pre_in ? pre * kLog2e : INFINITY) : (pre_in ? pre : 0.f);
+        if (i + 1 < n_iter) {
+          const float* src = stage_src(i + 1);
+          pre_in = src != nullptr;
+          if (pre_in) pre = __ldg(src);
         }
-        // All 256 compute threads have staged their value (and, through the
-        // previous iteration's wait, finished reading this slot two iterations ago).
-        mbar_arrive(bar(L::bLse + slot));
-        if (!(ok = wait_warp(bar(L::bLse + slot), (i >> 1) & 1, ctl))) break;
-
-        // The previous tile's dQ (overlaps this tile's S^T product).
-        if (i > 0 && !(ok = drain_dq(i - 1))) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bLse + 2 * half + slot));
+        if (!(ok = wait_warp(bar(L::bLse + 2 * half + slot), (i >> 1) & 1, ctl))) break;
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 4, i);
+        const float* lse_s = stage;
+        const float* dl_s = stage + 64;
 
         // P^T = exp(alpha S^T - lse) for this thread's 64 queries.
         const bool diag = CAUSAL && q0 == k0;
         if (!(ok = wait_warp(bar(L::bSFull), i & 1, ctl))) break;
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 6, i);
         tc_fence_after();
         uint32_t sv[64];
         tmem_ld64(tmem + L::kColS + lane_off + 64 * half, sv);
         tmem_ld_wait64(sv);
         float p[64];
-        const float4* l4 = reinterpret_cast<const float4*>(lse_s + slot * kTile + 64 * half);
+        const float4* l4 = reinterpret_cast<const float4*>(lse_s);
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const float4 lq = l4[u];
@@ -340,16 +411,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tmem + L::kColS + lane_off + 64 * half, pk);
         }
         tmem_st_wait();
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 7, i);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPReady));
 
+        // The previous tile's dQ; once drained, its product no longer reads the
+        // dS^T buffer that this tile's dS phase writes.
+        if (i > 0 && !(ok = drain_dq(i - 1))) break;
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 5, i);
+
         // dS^T = P^T o (dP^T - delta) (alpha is applied to dK and dQ at the end).
         if (!(ok = wait_warp(bar(L::bDPFull), i & 1, ctl))) break;
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 9, i);
         tc_fence_after();
         tmem_ld64(tmem + L::kColDP + lane_off + 64 * half, sv);
         tmem_ld_wait64(sv);
-        const float4* d4 = reinterpret_cast<const float4*>(dl_s + slot * kTile + 64 * half);
+        const float4* d4 = reinterpret_cast<const float4*>(dl_s);
         uint32_t pk[32];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -363,8 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[2 * u + 1] = pack_bf16x2(t2, t3);
         }
         tmem_st32(tmem + L::kColDP + lane_off + 64 * half, pk);
-        // dS^T row into the swizzled [keys][queries] buffer, panel `half`. The
-        // previous dQ product (its reader) completed before drain_dq returned.
+        // dS^T row into the swizzled [keys][queries] buffer, panel `half`.
         {
           const uint32_t rowb = sbase + L::kDS + half * L::kPanelBytes;
 #pragma unroll
@@ -373,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tmem_st_wait();
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 10, i);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bDSReady));
@@ -408,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    // Every dQ box this warp handed to the TMA unit has completed before the
+    // CTA's shared memory is released.
+    if (L::kTmaDQ) bulk_wait_all_warp();
     asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
   }
 
@@ -422,14 +503,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                         cudaStream_t stream) {
   using L = BwdLayout<D>;
   auto kern = attn_bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   const int n_t = (a.s.N + kTile - 1) / kTile;
   const dim3 grid(static_cast<unsigned>(n_t) * a.s.B * a.s.Hkv);
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -444,12 +526,13 @@ __global__ void convert_dq_kernel(const float4* __restrict__ src, uint2* __restr
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
+                       cudaStream_t stream) {
   if (a.s.d == 64)
-    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, a, stream)
-                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, a, stream);
-  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, a, stream)
-                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, a, stream);
+    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, a, stream)
+                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, a, stream);
+  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, a, stream)
+                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, a, stream);
 }
 
 // dQ = BF16(dQ workspace); n is a multiple of 4 (d is 64 or 128).

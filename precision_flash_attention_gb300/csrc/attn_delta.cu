@@ -123,56 +123,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (*abort_flag == 0) {
     if (warp == 0) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTileBytes);
+      // TMA producer (whole warp, one elected lane issues).
+      mbar_arrive_expect_tx_warp(bar(L::bQFull), 2 * L::kTileBytes);
+      for (int p = 0; p < D / 64; ++p) {
+        tma_load_3d_warp(sbase + L::kQ + p * L::kPanelBytes, &tmQ, bar(L::bQFull), p * 64, q0, bh);
+        tma_load_3d_warp(sbase + L::kDO + p * L::kPanelBytes, &tmdO, bar(L::bQFull), p * 64, q0, bh);
+      }
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!wait_warp(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
+        issued = j + 1;
+        mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
         for (int p = 0; p < D / 64; ++p) {
-          tma_load_3d(sbase + L::kQ + p * L::kPanelBytes, &tmQ, bar(L::bQFull), p * 64, q0, bh);
-          tma_load_3d(sbase + L::kDO + p * L::kPanelBytes, &tmdO, bar(L::bQFull), p * 64, q0, bh);
+          tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
+                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
+          tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
+                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
         }
-        int issued = 0;
-        for (int j = 0; j < n_kt; ++j) {
-          const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          if (!wait_thread(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
-          issued = j + 1;
-          mbar_arrive_expect_tx(bar(L::bKVFull + s), 2 * L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
-            tma_load_3d(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
-          }
-        }
-        wait_drain(bar(L::bQFull), 0, ctl);
-        for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
-          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
       }
+      wait_drain(bar(L::bQFull), 0, ctl);
+      for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
+        wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
     } else if (warp == 1) {
-      if (lane == 0) {
-        constexpr uint32_t id = idesc_bf16(128, 128, false, false);
-        bool ok = wait_thread(bar(L::bQFull), 0, ctl);
-        for (int j = 0; ok && j < n_kt; ++j) {
-          const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          if (!(ok = wait_thread(bar(L::bKVFull + s), ph, ctl))) break;
-          if (j > 0 && !(ok = wait_thread(bar(L::bSFree), (j - 1) & 1, ctl))) break;
-          tc_fence_after();
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tmem, sdesc_sw128(sbase + L::kQ + koff, 16, 1024),
-                      sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), id, kk > 0);
-          }
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tmem + 128, sdesc_sw128(sbase + L::kDO + koff, 16, 1024),
-                      sdesc_sw128(sbase + L::kV + s * L::kTileBytes + koff, 16, 1024), id, kk > 0);
-          }
-          umma_commit(bar(L::bSFull));
-          umma_commit(bar(L::bKVEmpty + s));
+      // MMA issuer (whole warp, one elected lane issues).
+      constexpr uint32_t id = idesc_bf16(128, 128, false, false);
+      bool ok = wait_warp(bar(L::bQFull), 0, ctl);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int s = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!(ok = wait_warp(bar(L::bKVFull + s), ph, ctl))) break;
+        if (j > 0 && !(ok = wait_warp(bar(L::bSFree), (j - 1) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          umma_bf16_warp(tmem, sdesc_sw128(sbase + L::kQ + koff, 16, 1024),
+                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), id, kk > 0);
         }
-        umma_commit(bar(L::bDrain));
-        wait_drain(bar(L::bDrain), 0, ctl);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          umma_bf16_warp(tmem + 128, sdesc_sw128(sbase + L::kDO + koff, 16, 1024),
+                         sdesc_sw128(sbase + L::kV + s * L::kTileBytes + koff, 16, 1024), id, kk > 0);
+        }
+        umma_commit_warp(bar(L::bSFull));
+        umma_commit_warp(bar(L::bKVEmpty + s));
       }
+      umma_commit_warp(bar(L::bDrain));
+      wait_drain(bar(L::bDrain), 0, ctl);
     } else {
       const uint32_t quarter = warp & 3;
       const int r = quarter * 32 + lane;

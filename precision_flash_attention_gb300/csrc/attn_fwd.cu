@@ -23,6 +23,10 @@
 // The tensor core runs S0_j, PV1_{j-1}, S1_j, PV0_j, ... so that each tile's
 // softmax overlaps the other tile's two products.
 #include "pfa_device.cuh"
+#include "pfa_trace.cuh"
+
+PFA_TRACE_BUFFER(g_pfa_fwd_trace);
+#define PFA_FWD_TRACE(slot, ev, j) PFA_TRACE_EVENT(g_pfa_fwd_trace, slot, ev, j)
 
 namespace pfa {
 namespace {
@@ -67,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  PFA_TRACE_DECL();
 
   const AttnShape& sh = args.s;
   const int N = sh.N;
@@ -123,93 +128,94 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (*abort_flag == 0) {
     if (warp == 0) {
-      // ---------------- TMA producer ----------------
-      if (lane == 0) {
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        mbar_arrive_expect_tx(bar(L::bQFull), (has1 ? 2 : 1) * L::kTileBytes);
-        for (int t = 0; t < (has1 ? 2 : 1); ++t)
-          for (int p = 0; p < D / 64; ++p)
-            tma_load_3d(sbase + L::kQ + t * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                        bar(L::bQFull), p * 64, (qt0 + t) * kTile, bh);
-        int issued = 0;
-        for (int j = 0; j < n_iter; ++j) {
-          const int s = j % L::kStages;
-          const uint32_t ph = (j / L::kStages) & 1;
-          if (!wait_thread(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
-          issued = j + 1;
-          mbar_arrive_expect_tx(bar(L::bKVFull + s), 2 * L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
-            tma_load_3d(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                        bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
-          }
+      // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+      tma_prefetch_desc_warp(&tmQ);
+      tma_prefetch_desc_warp(&tmK);
+      tma_prefetch_desc_warp(&tmV);
+      mbar_arrive_expect_tx_warp(bar(L::bQFull), (has1 ? 2 : 1) * L::kTileBytes);
+      for (int t = 0; t < (has1 ? 2 : 1); ++t)
+        for (int p = 0; p < D / 64; ++p)
+          tma_load_3d_warp(sbase + L::kQ + t * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                           bar(L::bQFull), p * 64, (qt0 + t) * kTile, bh);
+      int issued = 0;
+      for (int j = 0; j < n_iter; ++j) {
+        const int s = j % L::kStages;
+        const uint32_t ph = (j / L::kStages) & 1;
+        if (!wait_warp(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
+        issued = j + 1;
+        mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
+        for (int p = 0; p < D / 64; ++p) {
+          tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
+                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
+          tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
+                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
         }
-        // Drain: every issued copy has landed before shared memory is released.
-        wait_drain(bar(L::bQFull), 0, ctl);
-        for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
-          wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
       }
+      // Drain: every issued copy has landed before shared memory is released.
+      wait_drain(bar(L::bQFull), 0, ctl);
+      for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
+        wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
     } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
-      if (lane == 0) {
-        constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-        constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-        auto issue_s = [&](int t, int s) {
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-            umma_bf16(tmem + 128 * t, sdesc_sw128(sbase + L::kQ + t * L::kTileBytes + koff, 16, 1024),
-                      sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
-          }
-          umma_commit(bar(L::bSFull + t));
-        };
-        // Obar_t (+)= Pbar_t V_j; Pbar_t is columns [0, 64) of S_t, 8 columns per K step.
-        auto issue_pv = [&](int t, int s, int j) {
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a(tmem + 256 + D * t, tmem + 128 * t + 8 * kk,
-                             sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
-                                         L::kPanelBytes, 1024),
-                             idPV, (j > 0 || kk > 0) ? 1u : 0u);
-        };
-        bool ok = wait_thread(bar(L::bQFull), 0, ctl);
-        for (int j = 0; ok && j < n_iter; ++j) {
-          const int s = j % L::kStages;
-          if (!(ok = wait_thread(bar(L::bKVFull + s), (j / L::kStages) & 1, ctl))) break;
-          const bool act0 = j <= last0, act1 = j <= last1;
+      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          umma_bf16_warp(tmem + 128 * t, sdesc_sw128(sbase + L::kQ + t * L::kTileBytes + koff, 16, 1024),
+                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
+        }
+        umma_commit_warp(bar(L::bSFull + t));
+      };
+      // Obar_t (+)= Pbar_t V_j; Pbar_t is columns [0, 64) of S_t, 8 columns per K step.
+      auto issue_pv = [&](int t, int s, int j) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          umma_bf16_tmem_a_warp(tmem + 256 + D * t, tmem + 128 * t + 8 * kk,
+                                sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
+                                            L::kPanelBytes, 1024),
+                                idPV, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      bool ok = wait_warp(bar(L::bQFull), 0, ctl);
+      for (int j = 0; ok && j < n_iter; ++j) {
+        const int s = j % L::kStages;
+        if (!(ok = wait_warp(bar(L::bKVFull + s), (j / L::kStages) & 1, ctl))) break;
+        const bool act0 = j <= last0, act1 = j <= last1;
+        if (lane == 0) PFA_FWD_TRACE(0, 1, j);
+        tc_fence_after();
+        if (act0) issue_s(0, s);
+        if (j > 0 && j - 1 <= last1) {
+          if (!(ok = wait_warp(bar(L::bPFull + 1), (j - 1) & 1, ctl))) break;
+          if (lane == 0) PFA_FWD_TRACE(0, 2, j - 1);
           tc_fence_after();
-          if (act0) issue_s(0, s);
-          if (j > 0 && j - 1 <= last1) {
-            if (!(ok = wait_thread(bar(L::bPFull + 1), (j - 1) & 1, ctl))) break;
-            tc_fence_after();
-            const int sp = (j - 1) % L::kStages;
-            issue_pv(1, sp, j - 1);
-            umma_commit(bar(L::bKVEmpty + sp));
-            if (j - 1 == last1) umma_commit(bar(L::bODone + 1));
-          }
-          if (act1) issue_s(1, s);
-          if (act0) {
-            if (!(ok = wait_thread(bar(L::bPFull + 0), j & 1, ctl))) break;
-            tc_fence_after();
-            issue_pv(0, s, j);
-            if (j == last0) umma_commit(bar(L::bODone + 0));
-            if (!act1) umma_commit(bar(L::bKVEmpty + s));
-          }
+          const int sp = (j - 1) % L::kStages;
+          issue_pv(1, sp, j - 1);
+          umma_commit_warp(bar(L::bKVEmpty + sp));
+          if (j - 1 == last1) umma_commit_warp(bar(L::bODone + 1));
         }
-        if (ok && last1 == n_iter - 1) {
-          const int j = n_iter - 1;
-          if ((ok = wait_thread(bar(L::bPFull + 1), j & 1, ctl))) {
-            tc_fence_after();
-            issue_pv(1, j % L::kStages, j);
-            umma_commit(bar(L::bKVEmpty + j % L::kStages));
-            umma_commit(bar(L::bODone + 1));
-          }
+        if (act1) issue_s(1, s);
+        if (act0) {
+          if (!(ok = wait_warp(bar(L::bPFull + 0), j & 1, ctl))) break;
+          if (lane == 0) PFA_FWD_TRACE(0, 3, j);
+          tc_fence_after();
+          issue_pv(0, s, j);
+          if (j == last0) umma_commit_warp(bar(L::bODone + 0));
+          if (!act1) umma_commit_warp(bar(L::bKVEmpty + s));
         }
-        // Drain: no MMA may still read shared memory or write TMEM at teardown.
-        umma_commit(bar(L::bDrain));
-        wait_drain(bar(L::bDrain), 0, ctl);
       }
+      if (ok && last1 == n_iter - 1) {
+        const int j = n_iter - 1;
+        if ((ok = wait_warp(bar(L::bPFull + 1), j & 1, ctl))) {
+          tc_fence_after();
+          issue_pv(1, j % L::kStages, j);
+          umma_commit_warp(bar(L::bKVEmpty + j % L::kStages));
+          umma_commit_warp(bar(L::bODone + 1));
+        }
+      }
+      // Drain: no MMA may still read shared memory or write TMEM at teardown.
+      umma_commit_warp(bar(L::bDrain));
+      wait_drain(bar(L::bDrain), 0, ctl);
     }
     }
     __syncwarp();
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int k0 = j * kTile;
         const bool need_mask = (CAUSAL && k0 + kTile > q0) || (k0 + kTile > N);
         if (!(ok = wait_warp(bar(L::bSFull + t), j & 1, ctl))) break;
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 4, j);
         tc_fence_after();
         uint32_t v[128];
         tmem_ld64(tS, v);
@@ -292,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m1_old = m1;
         m1 = fmaxf(m1, t1);
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 5, j);
 
         // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
         // repeats within eps change their shift.
@@ -328,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 6, j);
         // Pbar = exp(S - m) in FP32; l sums it; the BF16 cast goes to TMEM over S.
         const float nml2 = -m_sh * kLog2e;
         const float thr = m1 - args.tau_raw;
@@ -350,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
         tmem_st_wait();
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 7, j);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPFull + t));

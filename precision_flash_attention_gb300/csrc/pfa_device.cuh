@@ -119,9 +119,13 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
+// Warp-collective: every lane calls it with the same arguments; one elected lane arrives.
+__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
+      "r"(bytes)
+      : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -167,22 +171,6 @@ __device__ __forceinline__ void raise_error(const WaitCtl& c, int code, uint32_t
   }
 }
 
-// Single-thread wait (producer / MMA issuer). Returns false on timeout/abort.
-__device__ __forceinline__ bool wait_thread(uint32_t bar, uint32_t parity, const WaitCtl& c) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (*c.abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        raise_error(c, PFA_DEVERR_TIMEOUT, bar, parity, false);
-        return false;
-      }
-    }
-  }
-}
-
 // Whole-warp wait with a warp-uniform result (all 32 lanes must call it).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c) {
   if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
@@ -221,20 +209,66 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, const 
 // ----------------------------------------------------------------------------
 // TMA
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+// Issue from a whole warp. The TMA and tcgen05 issue instructions below are
+// warp-collective wrappers: all 32 lanes of the warp call them together with
+// warp-uniform arguments and one lane, chosen by elect.sync, issues. Issuing
+// from a branch that only one lane takes instead leaves the compiler unable to
+// treat the operands as uniform, which was measured at roughly 65 cycles per
+// tcgen05.mma against 32-64 cycles of tensor work.
+__device__ __forceinline__ void tma_prefetch_desc_warp(const CUtensorMap* m) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e prefetch.tensormap [%0];\n\t}" ::"l"(reinterpret_cast<uint64_t>(m))
+      : "memory");
 }
 
 // 3-D tiled load: coordinates (x innermost, y, z) in elements; x must be a
 // multiple of 8 for 16-bit data (16-byte rule), which the callers guarantee by
 // only using x in {0, 64}.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                            int x, int y, int z) {
+__device__ __forceinline__ void tma_load_3d_warp(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                                 int x, int y, int z) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];\n\t}" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// 3-D tiled reduce-add of a shared-memory box into global memory (FP32 add
+// for an FP32 tensor map). Elements outside the tensor's extent are skipped.
+// The coordinates must be non-negative and x x 4 bytes a multiple of 16.
+// Warp-collective; the elected lane also commits the copy to its bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d_warp(const CUtensorMap* m, uint32_t src, int x, int y,
+                                                       int z) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];\n\t"
+      "@e cp.async.bulk.commit_group;\n\t}" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+// The elected lane waits until its committed bulk copies have finished reading
+// shared memory (read) or have completed (all); then the warp reconverges.
+__device__ __forceinline__ void bulk_wait_read_warp() {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.wait_group.read 0;\n\t}" ::
+          : "memory");
+  __syncwarp();
+}
+__device__ __forceinline__ void bulk_wait_all_warp() {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.wait_group 0;\n\t}" ::
+          : "memory");
+  __syncwarp();
+}
+
+// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ----------------------------------------------------------------------------
@@ -259,34 +293,39 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], BF16 inputs, FP32 accumulate.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[smem] * B[smem], BF16 inputs, FP32 accumulate (warp-collective).
+__device__ __forceinline__ void umma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p;\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: A is read from tensor memory (one row per lane,
-// two BF16 values per 32-bit column, lower K index in the low half).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
+// two BF16 values per 32-bit column, lower K index in the low half). Warp-collective.
+__device__ __forceinline__ void umma_bf16_tmem_a_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                      uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p;\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// Arrive once on `bar` when every tcgen05.mma issued so far by the elected lane
+// has completed (warp-collective; the same lane is elected for every call of a
+// converged warp, so it covers all MMAs the warp issued).
+__device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 // Instruction descriptor for kind::f16 with BF16 A/B and FP32 D.
