@@ -11,17 +11,18 @@
 // pass (priors.kr, the fix paragraph; bud-325 note, Results): P is recomputed
 // from the saved lse whatever shift the forward pass used.
 //
-// 384 threads in three warpgroups: warp 0 TMA producer, warp 1 TMEM owner and
-// tcgen05.mma issuer, warps 2-3 idle; warps 4-11 compute. Compute warp w owns
-// TMEM lane quarter w % 4 (32 keys) and query half (w - 4) / 4 (64 queries).
+// 640 threads in five warpgroups: warp 0 TMA producer, warp 1 TMEM owner and
+// tcgen05.mma issuer, warps 2-3 idle; warps 4-19 compute. Compute warp w owns
+// TMEM lane quarter w % 4 (32 keys) and query group (w - 4) / 4 (32 queries), so
+// each SM sub-partition runs four compute warps whose latencies overlap.
 // P^T and dS^T are cast to BF16 and written back into TMEM over S^T and dP^T
-// (each query half over its own input columns), where they are the A operands of
-// dV and dK; dS^T also goes to a 128B-swizzled
-// shared buffer that the dQ product reads as its (M = queries) A operand.
+// (each query group over its own input columns), where they are the A operands
+// of dV and dK; dS^T also goes to a 128B-swizzled shared buffer that the dQ
+// product reads as its (M = queries) A operand.
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d),
 // dQ [384,448) for d = 64 and over dP^T [128,256) for d = 128.
-// Tensor-core order per query tile: S^T, dP^T, dV, dK, dQ; the P phase of the
-// compute warps overlaps dP^T and the dS phase overlaps dV.
+// Tensor-core order per query tile i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1),
+// so the next tile's scores are ready when the compute warps finish dS(i).
 #include "pfa_device.cuh"
 #include "pfa_trace.cuh"
 
@@ -31,15 +32,15 @@ PFA_TRACE_BUFFER(g_pfa_bwd_trace);
 namespace pfa {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 640;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// P^T and dS^T (BF16, two per 32-bit column) are written by each query half into
-// the first 32 columns of that half's own 64 FP32 input columns, so one half never
-// overwrites values the other half has yet to load. Query step kk (16 queries,
-// 8 columns) therefore sits at column 8 kk for kk < 4 and 32 + 8 kk after.
+// P^T and dS^T (BF16, two per 32-bit column) are written by each query group
+// into the first 16 columns of that group's own 32 FP32 input columns, so no
+// group overwrites values another group has yet to load. Query step kk (16
+// queries, 8 columns) therefore sits at column 32 (kk / 2) + 8 (kk % 2).
 __host__ __device__ constexpr uint32_t packed_col(int kk) {
-  return 8u * static_cast<uint32_t>(kk) + (kk >= 4 ? 32u : 0u);
+  return 32u * static_cast<uint32_t>(kk >> 1) + 8u * static_cast<uint32_t>(kk & 1);
 }
 
 template <int D>
@@ -50,17 +51,21 @@ struct BwdLayout {
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kPanelBytes = kTile * 128;
   // dQ leaves through a TMA reduce-add from a per-warp staging box (d = 64:
-  // 32 rows x 32 FP32 columns, 4 KB per compute warp); d = 128 has no room left
-  // for the staging and reduce-adds with vector atomics.
+  // 32 rows x 16 FP32 columns with 64-byte swizzle, 2 KB per compute warp);
+  // d = 128 has no room left for the staging and reduce-adds with vector atomics.
   static constexpr bool kTmaDQ = (D == 64);
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileBytes;
   static constexpr int kQ = kV + kTileBytes;                // + stage * tile
   static constexpr int kDO = kQ + kStages * kTileBytes;     // + stage * tile
-  static constexpr int kDS = kDO + kStages * kTileBytes;    // dS^T [keys][queries] bf16, 2 panels
-  static constexpr int kDQStage = kDS + kTile * kTile * 2;  // 8 warps x 4 KB (d = 64 only)
-  static constexpr int kLse = kDQStage + (kTmaDQ ? 8 * 4096 : 0);  // [slot 2][half 2][lse 64 | delta 64]
-  static constexpr int kBars = kLse + 2 * 2 * 128 * 4;
+  // d = 64 double-buffers dS^T so that dS(i) need not wait until dQ(i-1) has read
+  // dS(i-1); that takes the dQ drain off the compute warps' critical path.
+  static constexpr bool kDSDouble = (D == 64);
+  static constexpr int kDSBytes = kTile * kTile * 2;
+  static constexpr int kDS = kDO + kStages * kTileBytes;    // dS^T [keys][queries] bf16, 2 panels (x 2)
+  static constexpr int kDQStage = kDS + (kDSDouble ? 2 : 1) * kDSBytes;  // 16 warps x 2 KB (d = 64 only)
+  static constexpr int kLse = kDQStage + (kTmaDQ ? 16 * 2048 : 0);  // [slot 2][group 4][-lse 32 | -delta 32]
+  static constexpr int kBars = kLse + 2 * 4 * 64 * 4;
   static constexpr int bKVFull = 0;
   static constexpr int bQFull = 1;                  // + stage
   static constexpr int bQEmpty = bQFull + kStages;  // + stage
@@ -70,8 +75,8 @@ struct BwdLayout {
   static constexpr int bDSReady = bPReady + 1;
   static constexpr int bDQFull = bDSReady + 1;
   static constexpr int bDQFree = bDQFull + 1;
-  static constexpr int bLse = bDQFree + 1;          // + 2 * half + slot
-  static constexpr int bMMADone = bLse + 4;
+  static constexpr int bLse = bDQFree + 1;          // + 2 * group + slot
+  static constexpr int bMMADone = bLse + 8;
   static constexpr int bDrain = bMMADone + 1;
   static constexpr int bRegs = bDrain + 1;          // the compute warps hold their registers
   static constexpr int kNumBars = bRegs + 1;
@@ -80,7 +85,8 @@ struct BwdLayout {
   static constexpr int kBytes = kAbort + 4;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kColDQ = (D == 64) ? 384 : 128;
-  static constexpr bool kDQAliasesDP = (D != 64);
+  // Without the second dS buffer (d = 128) dQ also shares the dP^T columns.
+  static_assert(kDSDouble ? (kColDQ >= kColDK + D) : (kColDQ == kColDP), "dQ columns");
   static_assert(kDQStage % 1024 == 0, "swizzled staging boxes need 1024-byte alignment");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
@@ -115,9 +121,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
   const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 2u};
-  // iteration -> (query head, query tile)
-  auto iter_head = [&](int i) { return b * sh.Hq + hk * group + i / per_head; };
-  auto iter_q0 = [&](int i) { return (qt_first + i % per_head) * kTile; };
+  // Iteration i covers query head (first head) + i / per_head and query tile
+  // qt_first + i % per_head; the roles step through that order with a cursor.
+  struct QCursor {
+    int bh, q0;
+  };
+  const QCursor first{b * sh.Hq + hk * group, qt_first * kTile};
+  auto advance = [&](QCursor c) {
+    c.q0 += kTile;
+    if (c.q0 >= n_t * kTile) {
+      c.q0 = qt_first * kTile;
+      ++c.bh;
+    }
+    return c;
+  };
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
@@ -129,14 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(L::bSFull), 1);
     mbar_init(bar(L::bDPFull), 1);
-    mbar_init(bar(L::bPReady), 8);
-    mbar_init(bar(L::bDSReady), 8);
+    mbar_init(bar(L::bPReady), 16);
+    mbar_init(bar(L::bDSReady), 16);
     mbar_init(bar(L::bDQFull), 1);
-    mbar_init(bar(L::bDQFree), 8);
-    for (int x = 0; x < 4; ++x) mbar_init(bar(L::bLse + x), 4);
+    mbar_init(bar(L::bDQFree), 16);
+    for (int x = 0; x < 8; ++x) mbar_init(bar(L::bLse + x), 4);
     mbar_init(bar(L::bMMADone), 1);
     mbar_init(bar(L::bDrain), 1);
-    mbar_init(bar(L::bRegs), 8);
+    mbar_init(bar(L::bRegs), 16);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -147,11 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Register split per warpgroup: launched with 168 per thread (384 x 168 =
-  // 64512); warpgroup 0 drops to 72 and the compute warpgroups rise to 216
-  // (128 x 72 + 256 x 216 = 64512); all return to 168 before the teardown.
+  // Register split per warpgroup: launched with 96 per thread (640 x 96 =
+  // 61440); warpgroup 0 drops to 56 and the compute warpgroups rise to 104
+  // (128 x 56 + 512 x 104 = 60416); all return to 96 before the teardown.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (*abort_flag == 0) {
       if (warp == 0) {
         // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
@@ -166,13 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d_warp(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
         }
         int issued = 0;
-        for (int i = 0; i < n_iter; ++i) {
+        QCursor pc = first;
+        for (int i = 0; i < n_iter; ++i, pc = advance(pc)) {
           const int s = i % L::kStages;
           const uint32_t ph = (i / L::kStages) & 1;
           if (!wait_warp(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
           issued = i + 1;
-          const int bhq = iter_head(i);
-          const int q0 = iter_q0(i);
+          const int bhq = pc.bh;
+          const int q0 = pc.q0;
           mbar_arrive_expect_tx_warp(bar(L::bQFull + s), 2 * L::kTileBytes);
           for (int p = 0; p < D / 64; ++p) {
             tma_load_3d_warp(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
@@ -186,7 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, ctl);
       } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-        // Order per query tile i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1). S^T(i+1)
+        // Order per query tile i: dV(i), S^T(i+1), dK(i), then dP^T(i+1) and dQ(i)
+        // (d = 64: dP^T first; d = 128, where dQ sits over dP^T: dQ first). S^T(i+1)
         // overwrites P^T(i) after dV(i) has read it and runs while the compute warps
         // form dS(i); dP^T(i+1) overwrites dS^T(i) after dK(i) has read it.
         constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T
@@ -249,20 +268,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kTile / 16; ++kk)
             umma_bf16_tmem_a_warp(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
                                   idKM, (i > 0 || kk > 0) ? 1u : 0u);
-          if (!L::kDQAliasesDP && i > 0 && !(ok = wait_warp(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
+          if constexpr (L::kDSDouble) {
+            // dP^T(i+1) overwrites dS^T(i) after dK(i); dQ(i) reads its own dS buffer
+            // and waits only until dQ(i-1) has been drained.
+            if (more) issue_dp(i + 1);
+            if (i > 0 && !(ok = wait_warp(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
+          }
           tc_fence_after();
+          const uint32_t sDS = sbase + L::kDS + (L::kDSDouble ? (i & 1) * L::kDSBytes : 0);
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_warp(tDQ, sdesc_sw128(sbase + L::kDS + kk * 2048, L::kPanelBytes, 1024),
+            umma_bf16_warp(tDQ, sdesc_sw128(sDS + kk * 2048, L::kPanelBytes, 1024),
                            sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
-          // dQ done also means the dS^T buffer and this Q / dO stage are free.
+          // dQ done also means this dS^T buffer and this Q / dO stage are free.
           umma_commit_warp(bar(L::bDQFull));
           umma_commit_warp(bar(L::bQEmpty + s));
-          if (more) {
-            // With dQ over the dP^T columns, dP^T(i+1) waits until dQ(i) is drained.
-            if (L::kDQAliasesDP && !(ok = wait_warp(bar(L::bDQFree), i & 1, ctl))) break;
-            tc_fence_after();
-            issue_dp(i + 1);
+          if constexpr (!L::kDSDouble) {
+            if (more) {
+              // dQ sits over the dP^T columns: dP^T(i+1) waits until dQ(i) is drained.
+              if (!(ok = wait_warp(bar(L::bDQFree), i & 1, ctl))) break;
+              tc_fence_after();
+              issue_dp(i + 1);
+            }
           }
         }
         umma_commit_warp(bar(L::bMMADone));
@@ -276,186 +303,204 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waiting for. Their arrival follows their first instruction, so this wait is
     // short; it is bounded like every other wait.
     wait_drain(bar(L::bRegs), 0, ctl);
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 96;" ::: "memory");
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::bRegs));
     if (*abort_flag == 0) {
       // ---------------- compute warps ----------------
       const uint32_t quarter = warp & 3;
-      const int half = (warp - 4) >> 2;          // query columns [64 half, 64 half + 64)
+      const int grp = (warp - 4) >> 2;           // query columns [32 grp, 32 grp + 32)
       const int r = quarter * 32 + lane;         // TMEM lane: key row (S^T, dP^T) / query row (dQ)
+      const int rg = r;                          // thread index within the group's 128
       const uint32_t lane_off = (quarter * 32u) << 16;
       const int key = k0 + r;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
-      constexpr int kDH = D / 2;                 // dQ / dK / dV columns per warp
-      const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 4) * 4096u;
+      constexpr int kDG = D / 4;                 // dQ / dK / dV columns per warp
+      const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 4) * 2048u;
       bool ok = true;
 
-      // Per-half staging of lse (x log2 e) and delta: slot [slot][half] holds the
-      // half's 64 lse values then its 64 deltas. Thread r of the half stages entry
-      // r; the value is loaded one iteration ahead so the load latency overlaps
-      // the previous tile.
-      auto stage_src = [&](int it) -> const float* {
-        const int q = iter_q0(it) + 64 * half + (r & 63);
+      // Per-group staging of -lse (x log2 e) and -delta: slot [slot][grp] holds
+      // the group's 32 values of -lse then its 32 values of -delta. Thread rg < 64
+      // of the group stages entry rg; the value is loaded one iteration ahead so
+      // the load latency overlaps the previous tile.
+      auto stage_src = [&](QCursor c) -> const float* {
+        if (rg >= 64) return nullptr;
+        const int q = c.q0 + 32 * grp + (rg & 31);
         if (q >= N) return nullptr;
-        const size_t off = static_cast<size_t>(iter_head(it)) * N + q;
-        return r < 64 ? args.lse + off : args.delta + off;
+        const size_t off = static_cast<size_t>(c.bh) * N + q;
+        return rg < 32 ? args.lse + off : args.delta + off;
       };
+      QCursor prv = first, cur = first, nxt = advance(first);
       float pre = 0.f;
       bool pre_in = false;
       if (n_iter > 0) {
-        const float* src = stage_src(0);
+        const float* src = stage_src(cur);
         pre_in = src != nullptr;
-        if (pre_in) pre = __ldg(src);
+        if (pre_in) pre = ld_global_early(src);
       }
 
       // dQ of iteration `it` from TMEM (this thread: query row q0 + r, columns
-      // [kDH half, kDH half + kDH)) -> alpha dQ reduce-added into the workspace.
-      auto drain_dq = [&](int it) -> bool {
+      // [kDG grp, kDG grp + kDG)) -> alpha dQ reduce-added into the workspace.
+      auto drain_dq = [&](int it, QCursor qc) -> bool {
         if (!wait_warp(bar(L::bDQFull), it & 1, ctl)) return false;
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 13, it);
         tc_fence_after();
         if constexpr (L::kTmaDQ) {
-          uint32_t v[32];
-          tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half, v);
-          tmem_ld_wait32(v);
+          uint32_t v[16];
+          tmem_ld16(tmem + L::kColDQ + lane_off + kDG * grp, v);
+          tmem_ld_wait16(v);
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 14, it);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::bDQFree));
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 19, it);
           // This warp's previous box has been read out of the staging buffer.
           bulk_wait_read_warp();
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 15, it);
+          // Row `lane` of the 64-byte-swizzled box: chunk c sits at c ^ ((lane / 2) % 4).
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(dq_stage + sw128_offset(lane, c),
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(dq_stage + lane * 64u + ((static_cast<uint32_t>(c) ^ ((lane >> 1) & 3u)) << 4),
                          __float_as_uint(alpha * __uint_as_float(v[4 * c + 0])),
                          __float_as_uint(alpha * __uint_as_float(v[4 * c + 1])),
                          __float_as_uint(alpha * __uint_as_float(v[4 * c + 2])),
                          __float_as_uint(alpha * __uint_as_float(v[4 * c + 3])));
           fence_proxy_async_smem();
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 16, it);
           __syncwarp();
-          tma_reduce_add_3d_warp(&tmdQ, dq_stage, kDH * half, iter_q0(it) + 32 * static_cast<int>(quarter),
-                                 iter_head(it));
+          tma_reduce_add_3d_warp(&tmdQ, dq_stage, kDG * grp, qc.q0 + 32 * static_cast<int>(quarter), qc.bh);
         } else {
-          const int q = iter_q0(it) + r;
-          float* dq_row = args.dq_accum + (static_cast<size_t>(iter_head(it)) * N + q) * D + kDH * half;
-#pragma unroll
-          for (int c = 0; c < kDH; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + L::kColDQ + lane_off + kDH * half + c, v);
-            tmem_ld_wait32(v);
-            if (q < N) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                atomicAdd(reinterpret_cast<float4*>(dq_row + c) + u,
-                          make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
-                                      alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
-            }
-          }
+          const int q = qc.q0 + r;
+          float* dq_row = args.dq_accum + (static_cast<size_t>(qc.bh) * N + q) * D + kDG * grp;
+          uint32_t v[32];
+          tmem_ld32(tmem + L::kColDQ + lane_off + kDG * grp, v);
+          tmem_ld_wait32(v);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(L::bDQFree));
+          if (q < N) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              atomicAdd(reinterpret_cast<float4*>(dq_row) + u,
+                        make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
+                                    alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
+          }
         }
         return true;
       };
 
-      for (int i = 0; ok && i < n_iter; ++i) {
-        const int q0 = iter_q0(i);
+      for (int i = 0; ok && i < n_iter; ++i, prv = cur, cur = nxt, nxt = advance(nxt)) {
+        const int q0 = cur.q0;
         const int slot = i & 1;
-        float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 2 + half) * 128;
-        // Entry r of this slot was last read two tiles ago; every warp of the half
-        // has passed the previous tile's wait since, so no one still reads it.
-        stage[r] = r < 64 ? (pre_in ? pre * kLog2e : INFINITY) : (pre_in ? pre : 0.f);
+        float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 4 + grp) * 64;
+        // Entry rg of this slot was last read two tiles ago; every warp of the
+        // group has passed the previous tile's wait since, so no one still reads it.
+        if (rg < 64) stage[rg] = rg < 32 ? (pre_in ? -pre * kLog2e : -INFINITY) : (pre_in ? -pre : 0.f);
         if (i + 1 < n_iter) {
-          const float* src = stage_src(i + 1);
+          const float* src = stage_src(nxt);
           pre_in = src != nullptr;
-          if (pre_in) pre = __ldg(src);
+          if (pre_in) pre = ld_global_early(src);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bLse + 2 * half + slot));
-        if (!(ok = wait_warp(bar(L::bLse + 2 * half + slot), (i >> 1) & 1, ctl))) break;
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 4, i);
-        const float* lse_s = stage;
-        const float* dl_s = stage + 64;
+        if (lane == 0) mbar_arrive(bar(L::bLse + 2 * grp + slot));
+        if (!(ok = wait_warp(bar(L::bLse + 2 * grp + slot), (i >> 1) & 1, ctl))) break;
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 4, i);
 
-        // P^T = exp(alpha S^T - lse) for this thread's 64 queries.
+        // P^T = exp(alpha S^T - lse) for this thread's 32 queries.
         const bool diag = CAUSAL && q0 == k0;
         if (!(ok = wait_warp(bar(L::bSFull), i & 1, ctl))) break;
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 6, i);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 6, i);
         tc_fence_after();
-        uint32_t sv[64];
-        tmem_ld64(tmem + L::kColS + lane_off + 64 * half, sv);
-        tmem_ld_wait64(sv);
-        float p[64];
-        const float4* l4 = reinterpret_cast<const float4*>(lse_s);
+        uint32_t sv[32];
+        tmem_ld32(tmem + L::kColS + lane_off + 32 * grp, sv);
+        tmem_ld_wait32(sv);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 11, i);
+        float p[32];
+        const float4* l4 = reinterpret_cast<const float4*>(stage);
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < 8; ++u) {
           const float4 lq = l4[u];
           fma2v(p[4 * u], p[4 * u + 1], __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]),
-                sl2, sl2, -lq.x, -lq.y);
+                sl2, sl2, lq.x, lq.y);
           fma2v(p[4 * u + 2], p[4 * u + 3], __uint_as_float(sv[4 * u + 2]),
-                __uint_as_float(sv[4 * u + 3]), sl2, sl2, -lq.z, -lq.w);
+                __uint_as_float(sv[4 * u + 3]), sl2, sl2, lq.z, lq.w);
         }
 #pragma unroll
-        for (int c = 0; c < 64; ++c) p[c] = ex2_approx(p[c]);
+        for (int c = 0; c < 32; ++c) p[c] = ex2_approx(p[c]);
         if (diag) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (q0 + 64 * half + c < key) p[c] = 0.f;
+          for (int c = 0; c < 32; ++c)
+            if (q0 + 32 * grp + c < key) p[c] = 0.f;
         }
         {
-          uint32_t pk[32];
+          uint32_t pk[16];
 #pragma unroll
-          for (int u = 0; u < 32; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
-          tmem_st32(tmem + L::kColS + lane_off + 64 * half, pk);
+          for (int u = 0; u < 16; ++u) pk[u] = pack_bf16x2(p[2 * u], p[2 * u + 1]);
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 12, i);
+          tmem_st16(tmem + L::kColS + lane_off + 32 * grp, pk);
         }
         tmem_st_wait();
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 7, i);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 7, i);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPReady));
 
-        // The previous tile's dQ; once drained, its product no longer reads the
-        // dS^T buffer that this tile's dS phase writes.
-        if (i > 0 && !(ok = drain_dq(i - 1))) break;
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 5, i);
+        // With one dS^T buffer the previous tile's dQ is drained first: once its
+        // product has completed it no longer reads the buffer this dS phase writes.
+        if constexpr (!L::kDSDouble) {
+          if (i > 0 && !(ok = drain_dq(i - 1, prv))) break;
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 5, i);
+        }
 
         // dS^T = P^T o (dP^T - delta) (alpha is applied to dK and dQ at the end).
         if (!(ok = wait_warp(bar(L::bDPFull), i & 1, ctl))) break;
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 9, i);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 9, i);
         tc_fence_after();
-        tmem_ld64(tmem + L::kColDP + lane_off + 64 * half, sv);
-        tmem_ld_wait64(sv);
-        const float4* d4 = reinterpret_cast<const float4*>(dl_s);
-        uint32_t pk[32];
+        tmem_ld32(tmem + L::kColDP + lane_off + 32 * grp, sv);
+        tmem_ld_wait32(sv);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 17, i);
+        const float4* d4 = reinterpret_cast<const float4*>(stage + 32);
+        uint32_t pk[16];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float4 dq = d4[u];
+        for (int u = 0; u < 8; ++u) {
+          const float4 nd = d4[u];
           float t0, t1, t2, t3;
-          fma2v(t0, t1, __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]), 1.f, 1.f, -dq.x, -dq.y);
-          fma2v(t2, t3, __uint_as_float(sv[4 * u + 2]), __uint_as_float(sv[4 * u + 3]), 1.f, 1.f, -dq.z, -dq.w);
+          fma2v(t0, t1, __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]), 1.f, 1.f, nd.x, nd.y);
+          fma2v(t2, t3, __uint_as_float(sv[4 * u + 2]), __uint_as_float(sv[4 * u + 3]), 1.f, 1.f, nd.z, nd.w);
           mul2v(t0, t1, t0, t1, p[4 * u], p[4 * u + 1]);
           mul2v(t2, t3, t2, t3, p[4 * u + 2], p[4 * u + 3]);
           pk[2 * u] = pack_bf16x2(t0, t1);
           pk[2 * u + 1] = pack_bf16x2(t2, t3);
         }
-        tmem_st32(tmem + L::kColDP + lane_off + 64 * half, pk);
-        // dS^T row into the swizzled [keys][queries] buffer, panel `half`.
+        tmem_st16(tmem + L::kColDP + lane_off + 32 * grp, pk);
+        // dS^T row into the swizzled [keys][queries] buffer: panel grp / 2, 16-byte
+        // chunks 4 (grp % 2) .. 4 (grp % 2) + 3 of the 128-byte row.
         {
-          const uint32_t rowb = sbase + L::kDS + half * L::kPanelBytes;
+          // dQ(i-2), the last reader of this buffer, completed before drain(i-2).
+          const uint32_t rowb =
+              sbase + L::kDS + (L::kDSDouble ? (i & 1) * L::kDSBytes : 0) + (grp >> 1) * L::kPanelBytes;
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            st_shared_v4(rowb + sw128_offset(r, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int c = 0; c < 4; ++c)
+            st_shared_v4(rowb + sw128_offset(r, 4 * (grp & 1) + c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
+                         pk[4 * c + 3]);
         }
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 18, i);
         fence_proxy_async_smem();
         tmem_st_wait();
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(1 + half, 10, i);
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 10, i);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bDSReady));
+        if constexpr (L::kDSDouble) {
+          if (i > 0 && !(ok = drain_dq(i - 1, prv))) break;
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 5, i);
+        }
       }
-      if (ok && n_iter > 0) ok = drain_dq(n_iter - 1);
+      // The loop's last step made prv the cursor of the final tile.
+      if (ok && n_iter > 0) ok = drain_dq(n_iter - 1, prv);
 
       // ---------------- epilogue: dK (x alpha), dV rows of this key tile ----------------
       if (ok) ok = wait_warp(bar(L::bMMADone), 0, ctl);
@@ -464,19 +509,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t row = static_cast<size_t>(bhk) * N + key;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
-          const uint32_t col = (which == 0 ? L::kColDK : L::kColDV) + kDH * half;
+          const uint32_t col = (which == 0 ? L::kColDK : L::kColDV) + kDG * grp;
           const float sc = which == 0 ? alpha : 1.f;
           __nv_bfloat16* out =
-              reinterpret_cast<__nv_bfloat16*>(which == 0 ? args.dk : args.dv) + row * D + kDH * half;
+              reinterpret_cast<__nv_bfloat16*>(which == 0 ? args.dk : args.dv) + row * D + kDG * grp;
 #pragma unroll 1
-          for (int c = 0; c < kDH; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + col + lane_off + c, v);
-            tmem_ld_wait32(v);
+          for (int c = 0; c < kDG; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + col + lane_off + c, v);
+            tmem_ld_wait16(v);
             if (key < N) {
               uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
+              for (int u = 0; u < 2; ++u)
                 dst[u] = make_uint4(pack_bf16x2(sc * __uint_as_float(v[8 * u + 0]), sc * __uint_as_float(v[8 * u + 1])),
                                     pack_bf16x2(sc * __uint_as_float(v[8 * u + 2]), sc * __uint_as_float(v[8 * u + 3])),
                                     pack_bf16x2(sc * __uint_as_float(v[8 * u + 4]), sc * __uint_as_float(v[8 * u + 5])),
@@ -489,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every dQ box this warp handed to the TMA unit has completed before the
     // CTA's shared memory is released.
     if (L::kTmaDQ) bulk_wait_all_warp();
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
   }
 
   tc_fence_before();
