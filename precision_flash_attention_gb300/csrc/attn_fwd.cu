@@ -243,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
 
-      float m1 = -INFINITY, m2 = -INFINITY;  // running top-2 of raw scores
+      float m1 = -INFINITY;                  // running maximum of raw scores
+      bool rep = false;                      // two entries within eps of m1
       float m_sh = -INFINITY;                // current shift, natural units
       float l0 = 0.f, l1 = 0.f;              // row sum of Pbar (two partial sums)
       int cnt = 0;                           // entries within tau of m1 (raw)
@@ -267,35 +268,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(key < N && (!CAUSAL || key <= qrow))) v[c] = __float_as_uint(-INFINITY);
           }
         }
-        // Tile maximum.
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+        // Tile maximum, as the maxima of eight blocks of 16 columns.
+        float bm[8];
 #pragma unroll
-        for (int c = 0; c < kTile; c += 8) {
-          a0 = fmax3(a0, __uint_as_float(v[c + 0]), __uint_as_float(v[c + 1]));
-          a1 = fmax3(a1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-          a2 = fmax3(a2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-          a3 = fmax3(a3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+        for (int k = 0; k < 8; ++k) {
+          auto x = [&](int e) { return __uint_as_float(v[16 * k + e]); };
+          const float u0 = fmax3(x(0), x(1), x(2)), u1 = fmax3(x(3), x(4), x(5));
+          const float u2 = fmax3(x(6), x(7), x(8)), u3 = fmax3(x(9), x(10), x(11));
+          const float u4 = fmax3(x(12), x(13), x(14));
+          bm[k] = fmaxf(fmax3(u0, u1, u2), fmax3(u3, u4, x(15)));
         }
-        const float t1 = fmax3(fmaxf(a0, a1), a2, a3);
-        // Second maximum (with multiplicity). A tile whose maximum stays below
-        // the running maximum contributes only that maximum to the top-2, so the
-        // sweep is needed only where a lane's maximum rises or ties.
+        const float t1 = fmax3(fmax3(bm[0], bm[1], bm[2]), fmax3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
+        // Repetition flag of the running row (at least two entries within eps of
+        // its maximum), kept exactly tile by tile without a second maximum:
+        //   new maximum t1 > m1: repeated iff m1 >= t1 - eps or this tile holds two
+        //                        entries >= t1 - eps;
+        //   m1 - eps <= t1 <= m1: repeated (an entry of this tile ties the maximum);
+        //   otherwise the flag is unchanged.
+        // Only rows whose maximum jumps by more than eps count entries, and only in
+        // the block that holds the new maximum when no other block reaches the
+        // threshold.
         if (kTies) {
-          float t2 = -INFINITY;
-          if (__any_sync(0xFFFFFFFFu, t1 >= m1)) {
-            float b0 = -INFINITY, b1 = -INFINITY;
-            int eq = 0;
-#pragma unroll
-            for (int c = 0; c < kTile; c += 2) {
-              const float x0 = __uint_as_float(v[c]), x1 = __uint_as_float(v[c + 1]);
-              const bool lt0 = x0 < t1, lt1 = x1 < t1;
-              eq += (lt0 ? 0 : 1) + (lt1 ? 0 : 1);
-              b0 = fmaxf(b0, lt0 ? x0 : -INFINITY);
-              b1 = fmaxf(b1, lt1 ? x1 : -INFINITY);
-            }
-            t2 = eq >= 2 ? t1 : fmaxf(b0, b1);
+          const float thr = t1 - args.eps_raw;
+          const bool jump = t1 > m1 && m1 < thr;
+          if (t1 > m1) {
+            rep = !jump;
+          } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
+            rep = true;
           }
-          m2 = fmax3(m2, t2, fminf(m1, t1));
+          if (__any_sync(0xFFFFFFFFu, jump)) {
+            int nb = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) nb += bm[k] >= thr ? 1 : 0;
+            if (jump) rep = nb >= 2;
+            const bool scan = jump && nb < 2;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const bool mine = scan && bm[k] >= thr;
+              if (__any_sync(0xFFFFFFFFu, mine)) {
+                int c = 0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) c += __uint_as_float(v[16 * k + e]) >= thr ? 1 : 0;
+                if (mine) rep = c >= 2;
+              }
+            }
+          }
         }
         const float m1_old = m1;
         m1 = fmaxf(m1, t1);
@@ -305,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // repeats within eps change their shift.
         const float r_m = m1 * alpha;
         float m_new = r_m;
-        if (MODE > 0 && (m1 - m2) <= args.eps_raw) {
+        if (MODE > 0 && rep) {
           if (MODE == 1)
             m_new = r_m > 0.f ? args.beta * r_m : (r_m < 0.f ? 0.f : kEpsShift);
           else
@@ -395,7 +412,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (row_ok) args.lse[static_cast<size_t>(bh) * N + qrow] = m_sh + lg2_approx(l) * kLn2;
         if (COUNT) {
-          const bool rep = (m1 - m2) <= args.eps_raw;
           // BF16(Pbar) == 1 under the final shift: entries within tau of m1,
           // unless the shift moved the maximum more than tau below zero.
           const float moved = m_sh - m1 * alpha;
