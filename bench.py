@@ -57,57 +57,120 @@ def dist_env():
     return world, rank, local
 
 
+class _NoClock:
+    """Stand-in for ClockSampler in profiling runs."""
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+    def wait_first(self, *a):
+        pass
+
+    def mark_start(self):
+        pass
+
+    def mark_end(self):
+        pass
+
+    def summary(self):
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks and throttle reasons sampled every 10 ms by a reader thread
+    that stamps each line with its arrival time. ``mark_start`` / ``mark_end``
+    bracket the timed region; the summary uses the samples inside it, and only if a
+    region is too short to hold one, the nearest sample on each side (both taken
+    under the same load: warm-up before, an untimed tail of steps after)."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 10
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.samples = []          # (host time, line)
+        self.t0 = self.t1 = None
+        self._thread = None
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            if ln.strip():
+                self.samples.append((time.perf_counter(), ln.strip()))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._thread = threading.Thread(target=self._reader, daemon=True)
+            self._thread.start()
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def wait_first(self, timeout_s=10.0):
+        """Block until sampling is live (or the tool is missing)."""
+        end = time.perf_counter() + timeout_s
+        while self.proc is not None and not self.samples and time.perf_counter() < end:
+            if self.proc.poll() is not None:
+                break
+            time.sleep(0.01)
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def __exit__(self, *exc):
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if self._thread is not None:
+                self._thread.join(timeout=5)
+
+    @staticmethod
+    def _parse(ln):
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            return None
+        try:
+            return float(parts[1]), float(parts[2]), parts[5:9]
+        except ValueError:
+            return None
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
+        parsed = [(t, self._parse(ln)) for t, ln in self.samples]
+        parsed = [(t, p) for t, p in parsed if p is not None]
+        if not parsed or self.t0 is None or self.t1 is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        inside = [p for t, p in parsed if self.t0 <= t <= self.t1]
+        window = "timed region"
+        if not inside:
+            before = [p for t, p in parsed if t < self.t0][-1:]
+            after = [p for t, p in parsed if t > self.t1][:1]
+            inside = before + after
+            window = "nearest samples around a timed region shorter than the sampling period"
+        reasons = set()
+        for _, _, flags in inside:
+            for n, v in zip(names, flags):
                 if v.lower() == "active":
                     reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(p[0] for p in inside), "sm_max_mhz": max(p[1] for p in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "window": window,
+                "period_ms": self.PERIOD_MS}
 
 
 def traffic_for(kernel: str):
@@ -126,6 +189,42 @@ def traffic_for(kernel: str):
         return e.get("dram_bytes_per_launch_full_workload")
     except (OSError, ValueError, KeyError):
         return None
+
+
+_SI = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+
+
+def write_traffic(csv_path: str, kernel: str, command: str) -> dict:
+    """Average DRAM bytes (read + write) per launch of `kernel` from an ncu --csv capture
+    of dram__bytes_read.sum and dram__bytes_write.sum, stored in profiles/traffic.json
+    under the digest of the current sources (so a later kernel change reads as null)."""
+    import csv
+    from precision_flash_attention_gb300 import build as _b
+    per_launch = {}
+    with open(csv_path, encoding="utf-8") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(lines):
+        if kernel not in row.get("Kernel Name", ""):
+            continue
+        name = row.get("Metric Name", "")
+        if name not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        val = float(row["Metric Value"].replace(",", "")) * _SI.get(row.get("Metric Unit", "byte"), 1.0)
+        per_launch[row["ID"]] = per_launch.get(row["ID"], 0.0) + val
+    if not per_launch:
+        raise SystemExit(f"no dram__bytes rows for {kernel} in {csv_path}")
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    data = {}
+    if os.path.exists(p):
+        with open(p, encoding="utf-8") as f:
+            data = json.load(f)
+    data[kernel] = {"dram_bytes_per_launch_full_workload": sum(per_launch.values()) / len(per_launch),
+                    "launches": len(per_launch), "source_digest": _b.source_digest(),
+                    "workload": dict(WORKLOAD), "command": command}
+    with open(p, "w", encoding="utf-8") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    return data[kernel]
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -279,17 +378,22 @@ def run_gpu_arm(args):
     head = args.mode
     steps = {m: Step(t, causal=w["causal"], scale=w["scale"], fix_mode=m, beta=w["beta"],
                      eps=w["eps"]) for m in sorted({0, head})}
-    for m in steps:
-        _progress(args, f"warm-up mode {m}")
-        time_step(steps[m], 1, args.warmup, flush)
-        _progress(args, f"warm-up mode {m} done, device error word {pfa.device_error()}")
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    # Interleave the modes so the cost of the fix is measured under the same conditions.
-    res = {m: {"fwd_ms": [], "delta_ms": [], "bwd_ms": [], "step_ms": []} for m in steps}
-    wall0 = time.perf_counter()
-    with ClockSampler(local) as clk:
+    # Clocks are sampled from before the warm-up (so sampling is live when timing
+    # starts) until after an untimed tail of the same steps; not under ncu.
+    clk = _NoClock() if args.kernels_only else ClockSampler(local)
+    with clk:
+        clk.wait_first()
+        for m in steps:
+            _progress(args, f"warm-up mode {m}")
+            time_step(steps[m], 1, args.warmup, flush)
+            _progress(args, f"warm-up mode {m} done, device error word {pfa.device_error()}")
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        # Interleave the modes so the cost of the fix is measured under the same conditions.
+        res = {m: {"fwd_ms": [], "delta_ms": [], "bwd_ms": [], "step_ms": []} for m in steps}
+        clk.mark_start()
+        wall0 = time.perf_counter()
         for it in range(args.steps):
             for m in steps:
                 r = time_step(steps[m], 1, 0, flush)
@@ -300,9 +404,18 @@ def run_gpu_arm(args):
                     _progress(args, f"step {it} mode {m}: {r['step_ms'][0]:.3f} ms, error word {err}"
                                     + (f", first timeout at {pfa.device_error_site()}" if err else ""))
         torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    wall = time.perf_counter() - wall0
+        if world > 1:
+            torch.distributed.barrier()
+        wall = time.perf_counter() - wall0
+        clk.mark_end()
+        # Untimed tail under the same load, so a sample follows a short timed region.
+        if not args.kernels_only:
+            tail0 = time.perf_counter()
+            for _ in range(2000):
+                time_step(steps[head], 1, 0, flush)
+                if time.perf_counter() - tail0 > 4 * ClockSampler.PERIOD_MS * 1e-3:
+                    break
+            torch.cuda.synchronize()
     assert pfa.device_error() == 0, "device error word set during the benchmark"
     if args.kernels_only:
         # Profiling run: the kernels above are all it launches (no sweep, copies or CPU work).
@@ -434,7 +547,14 @@ def main():
     ap.add_argument("--progress", action="store_true", help="log each stage to stderr")
     ap.add_argument("--kernels-only", action="store_true",
                     help="launch only the timed steps (for ncu captures); prints nothing")
+    ap.add_argument("--traffic-from", metavar="CSV",
+                    help="store the attn_bwd_kernel DRAM bytes per launch of an ncu --csv capture "
+                         "in profiles/traffic.json and exit (no GPU work)")
+    ap.add_argument("--traffic-command", default="", help="the ncu command line of that capture")
     args = ap.parse_args()
+    if args.traffic_from:
+        print(json.dumps(write_traffic(args.traffic_from, "attn_bwd_kernel", args.traffic_command)))
+        return
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         run_reference_arm(args)
