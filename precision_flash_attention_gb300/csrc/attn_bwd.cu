@@ -399,11 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Entry rg of this slot was last read two tiles ago; every warp of the
         // group has passed the previous tile's wait since, so no one still reads it.
         if (rg < 64) stage[rg] = rg < 32 ? (pre_in ? -pre * kLog2e : -INFINITY) : (pre_in ? -pre : 0.f);
-        if (i + 1 < n_iter) {
-          const float* src = stage_src(nxt);
-          pre_in = src != nullptr;
-          if (pre_in) pre = ld_global_early(src);
-        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bLse + 2 * grp + slot));
         if (!(ok = wait_warp(bar(L::bLse + 2 * grp + slot), (i >> 1) & 1, ctl))) break;
@@ -447,6 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPReady));
+        // Prefetch the next tile's entry here: an mbarrier arrive (a release)
+        // waits for the arriving lane's loads in flight, and the next arrive of
+        // this warp comes after the whole dS phase.
+        if (i + 1 < n_iter) {
+          const float* src = stage_src(nxt);
+          pre_in = src != nullptr;
+          if (pre_in) pre = ld_global_early(src);
+        }
 
         // With one dS^T buffer the previous tile's dQ is drained first: once its
         // product has completed it no longer reads the buffer this dS phase writes.
@@ -459,17 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_warp(bar(L::bDPFull), i & 1, ctl))) break;
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 9, i);
         tc_fence_after();
-        tmem_ld32(tmem + L::kColDP + lane_off + 32 * grp, sv);
-        tmem_ld_wait32(sv);
+        uint32_t dv[32];
+        tmem_ld32(tmem + L::kColDP + lane_off + 32 * grp, dv);
+        tmem_ld_wait32(dv);
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 17, i);
         const float4* d4 = reinterpret_cast<const float4*>(stage + 32);
         uint32_t pk[16];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const float4 nd = d4[u];
-          float t0, t1, t2, t3;
-          fma2v(t0, t1, __uint_as_float(sv[4 * u]), __uint_as_float(sv[4 * u + 1]), 1.f, 1.f, nd.x, nd.y);
-          fma2v(t2, t3, __uint_as_float(sv[4 * u + 2]), __uint_as_float(sv[4 * u + 3]), 1.f, 1.f, nd.z, nd.w);
+          float t0 = __uint_as_float(dv[4 * u]), t1 = __uint_as_float(dv[4 * u + 1]);
+          float t2 = __uint_as_float(dv[4 * u + 2]), t3 = __uint_as_float(dv[4 * u + 3]);
+          add2(t0, t1, nd.x, nd.y);
+          add2(t2, t3, nd.z, nd.w);
           mul2v(t0, t1, t0, t1, p[4 * u], p[4 * u + 1]);
           mul2v(t2, t3, t2, t3, p[4 * u + 2], p[4 * u + 3]);
           pk[2 * u] = pack_bf16x2(t0, t1);
