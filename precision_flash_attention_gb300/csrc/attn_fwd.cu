@@ -245,6 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m1 = -INFINITY;                  // running maximum of raw scores
       bool rep = false;                      // two entries within eps of m1
+      // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
+      // repeats within eps change their shift.
+      auto shift_of = [&](float mx, bool repeated) {
+        const float r_m = mx * alpha;
+        if (MODE == 0 || !repeated) return r_m;
+        if (MODE == 1) return r_m > 0.f ? args.beta * r_m : (r_m < 0.f ? 0.f : kEpsShift);
+        return r_m + kEpsShift;
+      };
       float m_sh = -INFINITY;                // current shift, natural units
       float l0 = 0.f, l1 = 0.f;              // row sum of Pbar (two partial sums)
       int cnt = 0;                           // entries within tau of m1 (raw)
@@ -285,49 +293,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         //                        entries >= t1 - eps;
         //   m1 - eps <= t1 <= m1: repeated (an entry of this tile ties the maximum);
         //   otherwise the flag is unchanged.
-        // Only rows whose maximum jumps by more than eps count entries, and only in
-        // the block that holds the new maximum when no other block reaches the
-        // threshold.
+        // The count of a tile whose maximum jumped by more than eps is taken after
+        // this tile's Pbar has been handed over (below), so this tile's shift uses
+        // "not repeated" for such a row and the next tile's shift the exact flag.
+        // An intermediate shift only changes this tile's BF16 rounding: Obar and l
+        // are rescaled whenever the shift moves, and the epilogue applies the
+        // exact final shift.
+        bool jump = false;
+        float thr_eps = 0.f;
         if (kTies) {
-          const float thr = t1 - args.eps_raw;
-          const bool jump = t1 > m1 && m1 < thr;
+          thr_eps = t1 - args.eps_raw;
+          jump = t1 > m1 && m1 < thr_eps;
           if (t1 > m1) {
             rep = !jump;
           } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
             rep = true;
-          }
-          if (__any_sync(0xFFFFFFFFu, jump)) {
-            int nb = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) nb += bm[k] >= thr ? 1 : 0;
-            if (jump) rep = nb >= 2;
-            const bool scan = jump && nb < 2;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const bool mine = scan && bm[k] >= thr;
-              if (__any_sync(0xFFFFFFFFu, mine)) {
-                int c = 0;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) c += __uint_as_float(v[16 * k + e]) >= thr ? 1 : 0;
-                if (mine) rep = c >= 2;
-              }
-            }
           }
         }
         const float m1_old = m1;
         m1 = fmaxf(m1, t1);
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 5, j);
 
-        // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
-        // repeats within eps change their shift.
-        const float r_m = m1 * alpha;
-        float m_new = r_m;
-        if (MODE > 0 && rep) {
-          if (MODE == 1)
-            m_new = r_m > 0.f ? args.beta * r_m : (r_m < 0.f ? 0.f : kEpsShift);
-          else
-            m_new = r_m + kEpsShift;
-        }
+        const float m_new = shift_of(m1, rep);
         const bool changed = (j > 0) && (m_new != m_sh);
         const float corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
         l0 *= corr;
@@ -380,12 +367,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+
+        // The deferred count: rows whose maximum jumped are repeated iff two of
+        // this tile's entries reach t1 - eps. Two blocks at or above it settle it;
+        // otherwise only the one block holding t1 is counted.
+        if (kTies && __any_sync(0xFFFFFFFFu, jump)) {
+          int nb = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
+          bool r2 = nb >= 2;
+          const bool scan = jump && nb < 2;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const bool mine = scan && bm[k] >= thr_eps;
+            if (__any_sync(0xFFFFFFFFu, mine)) {
+              int c = 0;
+#pragma unroll
+              for (int e = 0; e < 16; ++e) c += __uint_as_float(v[16 * k + e]) >= thr_eps ? 1 : 0;
+              if (mine) r2 = c >= 2;
+            }
+          }
+          if (jump) rep = r2;
+        }
       }
 
       // ---------------- epilogue ----------------
       if (ok && last >= 0) ok = wait_warp(bar(L::bODone + t), 0, ctl);
       if (ok && last >= 0) {
         tc_fence_after();
+        // The exact final shift; it differs from the one in use only when the last
+        // tile's deferred count turned the row repeated. Rescale as a tile would.
+        const float m_fin = shift_of(m1, rep);
+        const float fcorr = (MODE > 0 && m_fin != m_sh) ? ex2_approx((m_sh - m_fin) * kLog2e) : 1.f;
+        l0 *= fcorr;
+        l1 *= fcorr;
         const float l = l0 + l1;
         const bool row_ok = qrow < N;
         const float inv_l = 1.f / l;
@@ -400,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             float y0 = __uint_as_float(o[2 * u]), y1 = __uint_as_float(o[2 * u + 1]);
+            if (MODE > 0) mul2(y0, y1, fcorr);
             mul2(y0, y1, inv_l);
             pk[u] = pack_bf16x2(y0, y1);
           }
@@ -410,11 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[qd] = make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
           }
         }
-        if (row_ok) args.lse[static_cast<size_t>(bh) * N + qrow] = m_sh + lg2_approx(l) * kLn2;
+        if (row_ok) args.lse[static_cast<size_t>(bh) * N + qrow] = m_fin + lg2_approx(l) * kLn2;
         if (COUNT) {
           // BF16(Pbar) == 1 under the final shift: entries within tau of m1,
           // unless the shift moved the maximum more than tau below zero.
-          const float moved = m_sh - m1 * alpha;
+          const float moved = m_fin - m1 * alpha;
           long long c_rep = row_ok && rep ? 1 : 0;
           long long c_one = row_ok && moved <= args.tau_raw * alpha ? cnt : 0;
           long long c_nf = row_ok && !(l > 0.f && l < INFINITY) ? 1 : 0;
