@@ -96,18 +96,18 @@ int tile_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS ? PFA_OK : PFA_ERR_INVALID_ARG;
 }
 
-// [B*H, N, d] FP32 tensor (the dQ workspace), boxes of 16 columns (64 bytes,
-// 64B swizzle) x 32 rows: one backward compute warp's share of a dQ tile.
+// [B*H, N, d] FP32 tensor (the dQ workspace), boxes of 32 columns (128 bytes,
+// 128B swizzle) x 32 rows: half of one backward drain warp's share of a dQ tile.
 int f32_box_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                  static_cast<cuuint64_t>(N) * d * 4};
-  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t box[3] = {32, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PFA_OK : PFA_ERR_INVALID_ARG;
 }

@@ -1,6 +1,6 @@
-// Backward kernel. Per (key tile, batch, key/value head) one CTA loops over the
-// query heads that share the key/value head and over the query tiles, with all
-// five products on tcgen05 (FP32 accumulators in TMEM):
+// Backward kernel. A work item is one (key tile, batch, key/value head); it loops
+// over the query heads that share the key/value head and over the query tiles,
+// with all five products on tcgen05 (FP32 accumulators in TMEM):
 //   S^T  = K Q^T              P^T  = exp(alpha S^T - lse)      (recomputed)
 //   dP^T = V dO^T             dS^T = P^T o (dP^T - delta)      (alpha applied at the end)
 //   dV  += P^T dO             dK  += dS^T Q                    (stay in TMEM: no atomics)
@@ -11,10 +11,18 @@
 // pass (priors.kr, the fix paragraph; bud-325 note, Results): P is recomputed
 // from the saved lse whatever shift the forward pass used.
 //
-// 640 threads in five warpgroups: warp 0 TMA producer, warp 1 TMEM owner and
-// tcgen05.mma issuer, warps 2-3 idle; warps 4-19 compute. Compute warp w owns
-// TMEM lane quarter w % 4 (32 keys) and query group (w - 4) / 4 (32 queries), so
-// each SM sub-partition runs four compute warps whose latencies overlap.
+// Persistent: one CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+// in heavy-first order (key tile 0 has the most causal work). Barrier phases
+// count the CTA's query tiles across items, so an item's first products start
+// while the previous item's last dQ is drained and its dK / dV are stored, and
+// setup and teardown happen once per SM.
+//
+// 768 threads in six warpgroups: warp 0 Q / dO producer (TMA), warp 1 TMEM
+// owner and tcgen05.mma issuer, warp 2 K / V producer, warp 3 idle; warps 4-19
+// compute (P^T, dS^T); warps 20-23 drain dQ out of TMEM. Compute warp w owns TMEM lane quarter w % 4
+// (32 keys) and query group (w - 4) / 4 (32 queries), so each SM sub-partition
+// runs four compute warps whose latencies overlap; drain warp w owns query rows
+// of lane quarter w % 4 and all d columns of dQ.
 // P^T and dS^T are cast to BF16 and written back into TMEM over S^T and dP^T
 // (each query group over its own input columns), where they are the A operands
 // of dV and dK; dS^T also goes to a 128B-swizzled shared buffer that the dQ
@@ -32,7 +40,7 @@ PFA_TRACE_BUFFER(g_pfa_bwd_trace);
 namespace pfa {
 namespace {
 
-constexpr int kThreads = 640;
+constexpr int kThreads = 768;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // P^T and dS^T (BF16, two per 32-bit column) are written by each query group
@@ -63,11 +71,12 @@ struct BwdLayout {
   static constexpr bool kDSDouble = (D == 64);
   static constexpr int kDSBytes = kTile * kTile * 2;
   static constexpr int kDS = kDO + kStages * kTileBytes;    // dS^T [keys][queries] bf16, 2 panels (x 2)
-  static constexpr int kDQStage = kDS + (kDSDouble ? 2 : 1) * kDSBytes;  // 16 warps x 2 KB (d = 64 only)
+  static constexpr int kDQStage = kDS + (kDSDouble ? 2 : 1) * kDSBytes;  // 4 drain warps x 8 KB (d = 64 only)
   static constexpr int kLse = kDQStage + (kTmaDQ ? 16 * 2048 : 0);  // [slot 2][group 4][-lse 32 | -delta 32]
   static constexpr int kBars = kLse + 2 * 4 * 64 * 4;
-  static constexpr int bKVFull = 0;
-  static constexpr int bQFull = 1;                  // + stage
+  static constexpr int bKVFull = 0;                 // the item's K, V landed
+  static constexpr int bKVEmpty = bKVFull + 1;      // the item's last product read K, V
+  static constexpr int bQFull = bKVEmpty + 1;       // + stage
   static constexpr int bQEmpty = bQFull + kStages;  // + stage
   static constexpr int bSFull = bQEmpty + kStages;
   static constexpr int bDPFull = bSFull + 1;
@@ -76,7 +85,7 @@ struct BwdLayout {
   static constexpr int bDQFull = bDSReady + 1;
   static constexpr int bDQFree = bDQFull + 1;
   static constexpr int bLse = bDQFree + 1;          // + 2 * group + slot
-  static constexpr int bMMADone = bLse + 8;
+  static constexpr int bMMADone = bLse + 8;        // the item's products are done (dK, dV final)
   static constexpr int bDrain = bMMADone + 1;
   static constexpr int bRegs = bDrain + 1;          // the compute warps hold their registers
   static constexpr int kNumBars = bRegs + 1;
@@ -107,39 +116,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int N = sh.N;
   const int n_t = (N + kTile - 1) / kTile;
   const int BHkv = sh.B * sh.Hkv;
-  const int kt = static_cast<int>(blockIdx.x / BHkv);  // kt = 0 has the most causal work
-  const int bhk = blockIdx.x % BHkv;
-  const int b = bhk / sh.Hkv;
-  const int hk = bhk % sh.Hkv;
   const int group = sh.Hq / sh.Hkv;
-  const int k0 = kt * kTile;
-  const int qt_first = CAUSAL ? kt : 0;
-  const int per_head = n_t - qt_first;
-  const int n_iter = group * per_head;
+  const int n_items = n_t * BHkv;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
   const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 2u};
-  // Iteration i covers query head (first head) + i / per_head and query tile
-  // qt_first + i % per_head; the roles step through that order with a cursor.
+
+  // Work item -> key tile kt (item / BHkv: key tile 0, the heaviest, first) and
+  // (batch, key/value head). Its iterations cover query head bh0 + i / per_head
+  // and query tile qt_first + i % per_head; the roles step through them with a
+  // cursor.
+  struct Item {
+    int bhk, k0, qt_first, n_iter, bh0;
+  };
+  auto decode = [&](int item) {
+    Item it;
+    const int kt = item / BHkv;
+    it.bhk = item % BHkv;
+    it.k0 = kt * kTile;
+    it.qt_first = CAUSAL ? kt : 0;
+    it.n_iter = group * (n_t - it.qt_first);
+    it.bh0 = (it.bhk / sh.Hkv) * sh.Hq + (it.bhk % sh.Hkv) * group;
+    return it;
+  };
   struct QCursor {
     int bh, q0;
   };
-  const QCursor first{b * sh.Hq + hk * group, qt_first * kTile};
-  auto advance = [&](QCursor c) {
+  auto first_of = [&](const Item& it) { return QCursor{it.bh0, it.qt_first * kTile}; };
+  auto advance = [&](QCursor c, const Item& it) {
     c.q0 += kTile;
     if (c.q0 >= n_t * kTile) {
-      c.q0 = qt_first * kTile;
+      c.q0 = it.qt_first * kTile;
       ++c.bh;
     }
     return c;
   };
+  const int item0 = static_cast<int>(blockIdx.x);
+  const int stride = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
     if (sbase & 1023u) atomicOr(args.err, PFA_DEVERR_SMEM_ALIGN);
     mbar_init(bar(L::bKVFull), 1);
+    mbar_init(bar(L::bKVEmpty), 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::bQFull + s), 1);
       mbar_init(bar(L::bQEmpty + s), 1);
@@ -149,11 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::bPReady), 16);
     mbar_init(bar(L::bDSReady), 16);
     mbar_init(bar(L::bDQFull), 1);
-    mbar_init(bar(L::bDQFree), 16);
+    mbar_init(bar(L::bDQFree), 4);
     for (int x = 0; x < 8; ++x) mbar_init(bar(L::bLse + x), 4);
     mbar_init(bar(L::bMMADone), 1);
     mbar_init(bar(L::bDrain), 1);
-    mbar_init(bar(L::bRegs), 16);
+    mbar_init(bar(L::bRegs), 20);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -164,44 +185,68 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Register split per warpgroup: launched with 96 per thread (640 x 96 =
-  // 61440); warpgroup 0 drops to 56 and the compute warpgroups rise to 104
-  // (128 x 56 + 512 x 104 = 60416); all return to 96 before the teardown.
+  if (threadIdx.x == 32) PFA_BWD_TRACE(0, 30, 0);
+  // Register split per warpgroup: launched with 80 per thread (768 x 80 =
+  // 61440); warpgroup 0 and the drain warpgroup drop to 56 and the compute
+  // warpgroups rise to 88 (2 x 128 x 56 + 512 x 88 = 59392); all return to 80
+  // before the teardown.
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
     if (*abort_flag == 0) {
       if (warp == 0) {
-        // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
+        // ---------------- Q / dO producer (whole warp, one elected lane issues) ----------------
+        // One stream of query tiles across all items of this CTA.
         tma_prefetch_desc_warp(&tmQ);
-        tma_prefetch_desc_warp(&tmK);
-        tma_prefetch_desc_warp(&tmV);
         tma_prefetch_desc_warp(&tmdO);
         if (L::kTmaDQ) tma_prefetch_desc_warp(&tmdQ);
-        mbar_arrive_expect_tx_warp(bar(L::bKVFull), 2 * L::kTileBytes);
-        for (int p = 0; p < D / 64; ++p) {
-          tma_load_3d_warp(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, k0, bhk);
-          tma_load_3d_warp(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, k0, bhk);
-        }
-        int issued = 0;
-        QCursor pc = first;
-        for (int i = 0; i < n_iter; ++i, pc = advance(pc)) {
-          const int s = i % L::kStages;
-          const uint32_t ph = (i / L::kStages) & 1;
-          if (!wait_warp(bar(L::bQEmpty + s), ph ^ 1, ctl)) break;
-          issued = i + 1;
-          const int bhq = pc.bh;
-          const int q0 = pc.q0;
-          mbar_arrive_expect_tx_warp(bar(L::bQFull + s), 2 * L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d_warp(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                             bar(L::bQFull + s), p * 64, q0, bhq);
-            tma_load_3d_warp(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
-                             bar(L::bQFull + s), p * 64, q0, bhq);
+        int g = 0;        // query tiles issued by this CTA (all items)
+        bool ok = true;
+        for (int item = item0; ok && item < n_items; item += stride) {
+          const Item it = decode(item);
+          QCursor pc = first_of(it);
+          for (int i = 0; i < it.n_iter; ++i, ++g, pc = advance(pc, it)) {
+            const int s = g % L::kStages;
+            if (!(ok = wait_warp(bar(L::bQEmpty + s), ((g / L::kStages) & 1) ^ 1, ctl))) break;
+            mbar_arrive_expect_tx_warp(bar(L::bQFull + s), 2 * L::kTileBytes);
+            for (int p = 0; p < D / 64; ++p) {
+              tma_load_3d_warp(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                               bar(L::bQFull + s), p * 64, pc.q0, pc.bh);
+              tma_load_3d_warp(sbase + L::kDO + s * L::kTileBytes + p * L::kPanelBytes, &tmdO,
+                               bar(L::bQFull + s), p * 64, pc.q0, pc.bh);
+            }
           }
         }
-        wait_drain(bar(L::bKVFull), 0, ctl);
-        for (int i = issued > L::kStages ? issued - L::kStages : 0; i < issued; ++i)
+        // Every issued copy has landed before shared memory is released (earlier
+        // ones were consumed before later ones could reuse their stage).
+        for (int i = g > L::kStages ? g - L::kStages : 0; i < g; ++i)
           wait_drain(bar(L::bQFull + i % L::kStages), (i / L::kStages) & 1, ctl);
+      } else if (warp == 2) {
+        // ---------------- K / V producer: one pair per item ----------------
+        // The item's K and V once the previous item's last product has read
+        // theirs; the next item's pair is prefetched into L2 meanwhile.
+        tma_prefetch_desc_warp(&tmK);
+        tma_prefetch_desc_warp(&tmV);
+        int kv = 0;
+        bool ok = true;
+        for (int item = item0; item < n_items; item += stride) {
+          const Item it = decode(item);
+          if (kv > 0 && !(ok = wait_warp(bar(L::bKVEmpty), (kv - 1) & 1, ctl))) break;
+          mbar_arrive_expect_tx_warp(bar(L::bKVFull), 2 * L::kTileBytes);
+          for (int p = 0; p < D / 64; ++p) {
+            tma_load_3d_warp(sbase + L::kK + p * L::kPanelBytes, &tmK, bar(L::bKVFull), p * 64, it.k0, it.bhk);
+            tma_load_3d_warp(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, it.k0, it.bhk);
+          }
+          ++kv;
+          if (item + stride < n_items) {
+            const Item nx = decode(item + stride);
+            for (int p = 0; p < D / 64; ++p) {
+              tma_prefetch_l2_3d_warp(&tmK, p * 64, nx.k0, nx.bhk);
+              tma_prefetch_l2_3d_warp(&tmV, p * 64, nx.k0, nx.bhk);
+            }
+          }
+        }
+        if (kv > 0) wait_drain(bar(L::bKVFull), (kv - 1) & 1, ctl);
+        (void)ok;
       } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
         // Order per query tile i: dV(i), S^T(i+1), dK(i), then dP^T(i+1) and dQ(i)
@@ -234,65 +279,80 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma_commit_warp(bar(L::bDPFull));
         };
-        bool ok = wait_warp(bar(L::bKVFull), 0, ctl);
-        if (ok && n_iter > 0 && (ok = wait_warp(bar(L::bQFull), 0, ctl))) {
+        // The stage of query tile g (counted across items) is g % kStages.
+        int g = 0;
+        int kv = 0;
+        bool ok = true;
+        for (int item = item0; ok && item < n_items; item += stride, ++kv) {
+          const Item it = decode(item);
+          if (!(ok = wait_warp(bar(L::bKVFull), kv & 1, ctl))) break;
+          if (!(ok = wait_warp(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl))) break;
+          // With dQ over the dP^T columns (d = 128), dP^T(0) waits until the
+          // previous item's last dQ has been drained.
+          if (!L::kDSDouble && g > 0 && !(ok = wait_warp(bar(L::bDQFree), (g - 1) & 1, ctl))) break;
           tc_fence_after();
-          issue_s(0);
-          issue_dp(0);
-        }
-        for (int i = 0; ok && i < n_iter; ++i) {
-          const int s = i % L::kStages;
-          const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
-          const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
-          const bool more = i + 1 < n_iter;
-          // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
-          if (!(ok = wait_warp(bar(L::bPReady), i & 1, ctl))) break;
-          if (lane == 0) PFA_BWD_TRACE(0, 2, i);
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a_warp(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
-                                  idKM, (i > 0 || kk > 0) ? 1u : 0u);
-          if (more) {
-            const int s1 = (i + 1) % L::kStages;
-            if (!(ok = wait_warp(bar(L::bQFull + s1), ((i + 1) / L::kStages) & 1, ctl))) break;
-            if (lane == 0) PFA_BWD_TRACE(0, 1, i + 1);
+          issue_s(g);
+          issue_dp(g);
+          for (int i = 0; ok && i < it.n_iter; ++i) {
+            const int gg = g + i;
+            const int s = gg % L::kStages;
+            const uint32_t sQ = sbase + L::kQ + s * L::kTileBytes;
+            const uint32_t sDO = sbase + L::kDO + s * L::kTileBytes;
+            const bool more = i + 1 < it.n_iter;
+            // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
+            if (!(ok = wait_warp(bar(L::bPReady), gg & 1, ctl))) break;
+            if (lane == 0) PFA_BWD_TRACE(0, 2, gg);
             tc_fence_after();
-            issue_s(i + 1);
-          }
-          // dK += dS^T Q : A = dS^T in TMEM; dQ = dS K : A = dS^T smem read MN-major.
-          if (!(ok = wait_warp(bar(L::bDSReady), i & 1, ctl))) break;
-          if (lane == 0) PFA_BWD_TRACE(0, 3, i);
-          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a_warp(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
-                                  idKM, (i > 0 || kk > 0) ? 1u : 0u);
-          if constexpr (L::kDSDouble) {
-            // dP^T(i+1) overwrites dS^T(i) after dK(i); dQ(i) reads its own dS buffer
-            // and waits only until dQ(i-1) has been drained.
-            if (more) issue_dp(i + 1);
-            if (i > 0 && !(ok = wait_warp(bar(L::bDQFree), (i - 1) & 1, ctl))) break;
-          }
-          tc_fence_after();
-          const uint32_t sDS = sbase + L::kDS + (L::kDSDouble ? (i & 1) * L::kDSBytes : 0);
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_warp(tDQ, sdesc_sw128(sDS + kk * 2048, L::kPanelBytes, 1024),
-                           sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
-          // dQ done also means this dS^T buffer and this Q / dO stage are free.
-          umma_commit_warp(bar(L::bDQFull));
-          umma_commit_warp(bar(L::bQEmpty + s));
-          if constexpr (!L::kDSDouble) {
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16_tmem_a_warp(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
+                                    idKM, (i > 0 || kk > 0) ? 1u : 0u);
             if (more) {
-              // dQ sits over the dP^T columns: dP^T(i+1) waits until dQ(i) is drained.
-              if (!(ok = wait_warp(bar(L::bDQFree), i & 1, ctl))) break;
+              const int s1 = (gg + 1) % L::kStages;
+              if (!(ok = wait_warp(bar(L::bQFull + s1), ((gg + 1) / L::kStages) & 1, ctl))) break;
+              if (lane == 0) PFA_BWD_TRACE(0, 1, gg + 1);
               tc_fence_after();
-              issue_dp(i + 1);
+              issue_s(gg + 1);
+            }
+            // dK += dS^T Q : A = dS^T in TMEM; dQ = dS K : A = dS^T smem read MN-major.
+            if (!(ok = wait_warp(bar(L::bDSReady), gg & 1, ctl))) break;
+            if (lane == 0) PFA_BWD_TRACE(0, 3, gg);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16_tmem_a_warp(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
+                                    idKM, (i > 0 || kk > 0) ? 1u : 0u);
+            // dK(i) is the last reader of this Q / dO stage (dQ reads dS and K).
+            umma_commit_warp(bar(L::bQEmpty + s));
+            if constexpr (L::kDSDouble) {
+              // dP^T(i+1) overwrites dS^T(i) after dK(i) has read it; dQ(i) reads its
+              // own dS buffer and waits only until dQ(i-1) has left TMEM.
+              if (more) issue_dp(gg + 1);
+              if (gg > 0 && !(ok = wait_warp(bar(L::bDQFree), (gg - 1) & 1, ctl))) break;
+            }
+            tc_fence_after();
+            const uint32_t sDS = sbase + L::kDS + (L::kDSDouble ? (gg & 1) * L::kDSBytes : 0);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              umma_bf16_warp(tDQ, sdesc_sw128(sDS + kk * 2048, L::kPanelBytes, 1024),
+                             sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
+            umma_commit_warp(bar(L::bDQFull));
+            if constexpr (!L::kDSDouble) {
+              if (more) {
+                // dQ sits over the dP^T columns: dP^T(i+1) waits until dQ(i) is drained.
+                if (!(ok = wait_warp(bar(L::bDQFree), gg & 1, ctl))) break;
+                tc_fence_after();
+                issue_dp(gg + 1);
+              }
             }
           }
+          g += it.n_iter;
+          // The item's products are done once these commits arrive: dK / dV are
+          // final and K / V may be replaced.
+          if (lane == 0) PFA_BWD_TRACE(0, 31, kv);
+          umma_commit_warp(bar(L::bMMADone));
+          umma_commit_warp(bar(L::bKVEmpty));
         }
-        umma_commit_warp(bar(L::bMMADone));
         umma_commit_warp(bar(L::bDrain));
         wait_drain(bar(L::bDrain), 0, ctl);
       }
@@ -303,9 +363,87 @@ __global__ void __launch_bounds__(kThreads, 1)
     // waiting for. Their arrival follows their first instruction, so this wait is
     // short; it is bounded like every other wait.
     wait_drain(bar(L::bRegs), 0, ctl);
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 96;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 80;" ::: "memory");
+  } else if (warp >= 20) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bRegs));
+    if (*abort_flag == 0) {
+      // ---------------- drain warps: dQ(i) out of TMEM, alpha dQ into the workspace ----------------
+      const uint32_t quarter = warp & 3;
+      const uint32_t lane_off = (quarter * 32u) << 16;
+      const float alpha = sh.scale;
+      const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 20) * 8192u;
+      bool ok = true;
+      int g = 0;
+      for (int item = item0; ok && item < n_items; item += stride) {
+        const Item itm = decode(item);
+        QCursor qc = first_of(itm);
+        for (int i = 0; ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
+        const int it = g;
+        if (!(ok = wait_warp(bar(L::bDQFull), it & 1, ctl))) break;
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(3, 13, it);
+        tc_fence_after();
+        if constexpr (L::kTmaDQ) {
+          // Two 32 x 32 FP32 boxes (128-byte swizzle) per warp; the previous
+          // tile's boxes have been read out before they are rewritten.
+          bulk_wait_read_warp();
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + L::kColDQ + lane_off + 32 * c, v);
+            tmem_ld_wait32(v);
+            if (c == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(L::bDQFree));
+            }
+            const uint32_t box = dq_stage + 4096u * c;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              st_shared_v4(box + sw128_offset(lane, u), __float_as_uint(alpha * __uint_as_float(v[4 * u + 0])),
+                           __float_as_uint(alpha * __uint_as_float(v[4 * u + 1])),
+                           __float_as_uint(alpha * __uint_as_float(v[4 * u + 2])),
+                           __float_as_uint(alpha * __uint_as_float(v[4 * u + 3])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int y = qc.q0 + 32 * static_cast<int>(quarter);
+          tma_reduce_add_3d_warp(&tmdQ, dq_stage, 0, y, qc.bh);
+          tma_reduce_add_3d_warp(&tmdQ, dq_stage + 4096u, 32, y, qc.bh);
+        } else {
+          const int q = qc.q0 + static_cast<int>(quarter) * 32 + lane;
+          float* dq_row = args.dq_accum + (static_cast<size_t>(qc.bh) * N + q) * D;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + L::kColDQ + lane_off + 32 * c, v);
+            tmem_ld_wait32(v);
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar(L::bDQFree));
+            }
+            if (q < N) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                atomicAdd(reinterpret_cast<float4*>(dq_row + 32 * c) + u,
+                          make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
+                                      alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
+            }
+          }
+        }
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(3, 5, it);
+        }
+      }
+    }
+    // Every dQ box handed to the TMA unit has completed before the CTA's shared
+    // memory is released; registers are reclaimed as warpgroup 0 does.
+    if (L::kTmaDQ) bulk_wait_all_warp();
+    wait_drain(bar(L::bRegs), 0, ctl);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 80;" ::: "memory");
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 88;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::bRegs));
     if (*abort_flag == 0) {
@@ -315,11 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = quarter * 32 + lane;         // TMEM lane: key row (S^T, dP^T) / query row (dQ)
       const int rg = r;                          // thread index within the group's 128
       const uint32_t lane_off = (quarter * 32u) << 16;
-      const int key = k0 + r;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
       constexpr int kDG = D / 4;                 // dQ / dK / dV columns per warp
-      const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 4) * 2048u;
       bool ok = true;
 
       // Per-group staging of -lse (x log2 e) and -delta: slot [slot][grp] holds
@@ -333,80 +469,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t off = static_cast<size_t>(c.bh) * N + q;
         return rg < 32 ? args.lse + off : args.delta + off;
       };
-      QCursor prv = first, cur = first, nxt = advance(first);
       float pre = 0.f;
       bool pre_in = false;
-      if (n_iter > 0) {
-        const float* src = stage_src(cur);
+      if (item0 < n_items) {
+        const float* src = stage_src(first_of(decode(item0)));
         pre_in = src != nullptr;
         if (pre_in) pre = ld_global_early(src);
       }
 
-      // dQ of iteration `it` from TMEM (this thread: query row q0 + r, columns
-      // [kDG grp, kDG grp + kDG)) -> alpha dQ reduce-added into the workspace.
-      auto drain_dq = [&](int it, QCursor qc) -> bool {
-        if (!wait_warp(bar(L::bDQFull), it & 1, ctl)) return false;
-        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 13, it);
-        tc_fence_after();
-        if constexpr (L::kTmaDQ) {
-          uint32_t v[16];
-          tmem_ld16(tmem + L::kColDQ + lane_off + kDG * grp, v);
-          tmem_ld_wait16(v);
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 14, it);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::bDQFree));
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 19, it);
-          // This warp's previous box has been read out of the staging buffer.
-          bulk_wait_read_warp();
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 15, it);
-          // Row `lane` of the 64-byte-swizzled box: chunk c sits at c ^ ((lane / 2) % 4).
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            st_shared_v4(dq_stage + lane * 64u + ((static_cast<uint32_t>(c) ^ ((lane >> 1) & 3u)) << 4),
-                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 0])),
-                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 1])),
-                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 2])),
-                         __float_as_uint(alpha * __uint_as_float(v[4 * c + 3])));
-          fence_proxy_async_smem();
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 16, it);
-          __syncwarp();
-          tma_reduce_add_3d_warp(&tmdQ, dq_stage, kDG * grp, qc.q0 + 32 * static_cast<int>(quarter), qc.bh);
-        } else {
-          const int q = qc.q0 + r;
-          float* dq_row = args.dq_accum + (static_cast<size_t>(qc.bh) * N + q) * D + kDG * grp;
-          uint32_t v[32];
-          tmem_ld32(tmem + L::kColDQ + lane_off + kDG * grp, v);
-          tmem_ld_wait32(v);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::bDQFree));
-          if (q < N) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              atomicAdd(reinterpret_cast<float4*>(dq_row) + u,
-                        make_float4(alpha * __uint_as_float(v[4 * u]), alpha * __uint_as_float(v[4 * u + 1]),
-                                    alpha * __uint_as_float(v[4 * u + 2]), alpha * __uint_as_float(v[4 * u + 3])));
-          }
-        }
-        return true;
-      };
-
-      for (int i = 0; ok && i < n_iter; ++i, prv = cur, cur = nxt, nxt = advance(nxt)) {
+      int g = 0;   // query tiles of this CTA so far (all items): the barrier phases
+      for (int item = item0, kv = 0; ok && item < n_items; item += stride, ++kv) {
+      const Item itm = decode(item);
+      const int k0 = itm.k0;
+      const int key = k0 + r;
+      QCursor cur = first_of(itm);
+      for (int i = 0; ok && i < itm.n_iter; ++i, ++g) {
+        const int gi = g;
         const int q0 = cur.q0;
-        const int slot = i & 1;
+        // The next query tile: this item's next one or the next item's first.
+        const bool has_nxt = i + 1 < itm.n_iter || item + stride < n_items;
+        const QCursor nxt = i + 1 < itm.n_iter ? advance(cur, itm) : first_of(decode(item + stride));
+        const int slot = gi & 1;
         float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 4 + grp) * 64;
         // Entry rg of this slot was last read two tiles ago; every warp of the
         // group has passed the previous tile's wait since, so no one still reads it.
         if (rg < 64) stage[rg] = rg < 32 ? (pre_in ? -pre * kLog2e : -INFINITY) : (pre_in ? -pre : 0.f);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bLse + 2 * grp + slot));
-        if (!(ok = wait_warp(bar(L::bLse + 2 * grp + slot), (i >> 1) & 1, ctl))) break;
+        if (!(ok = wait_warp(bar(L::bLse + 2 * grp + slot), (gi >> 1) & 1, ctl))) break;
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 4, i);
 
         // P^T = exp(alpha S^T - lse) for this thread's 32 queries.
         const bool diag = CAUSAL && q0 == k0;
-        if (!(ok = wait_warp(bar(L::bSFull), i & 1, ctl))) break;
+        if (!(ok = wait_warp(bar(L::bSFull), gi & 1, ctl))) break;
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 6, i);
         tc_fence_after();
         uint32_t sv[32];
@@ -445,21 +540,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Prefetch the next tile's entry here: an mbarrier arrive (a release)
         // waits for the arriving lane's loads in flight, and the next arrive of
         // this warp comes after the whole dS phase.
-        if (i + 1 < n_iter) {
+        if (has_nxt) {
           const float* src = stage_src(nxt);
           pre_in = src != nullptr;
           if (pre_in) pre = ld_global_early(src);
         }
 
-        // With one dS^T buffer the previous tile's dQ is drained first: once its
-        // product has completed it no longer reads the buffer this dS phase writes.
-        if constexpr (!L::kDSDouble) {
-          if (i > 0 && !(ok = drain_dq(i - 1, prv))) break;
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 5, i);
-        }
 
         // dS^T = P^T o (dP^T - delta) (alpha is applied to dK and dQ at the end).
-        if (!(ok = wait_warp(bar(L::bDPFull), i & 1, ctl))) break;
+        if (!(ok = wait_warp(bar(L::bDPFull), gi & 1, ctl))) break;
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 9, i);
         tc_fence_after();
         uint32_t dv[32];
@@ -484,9 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dS^T row into the swizzled [keys][queries] buffer: panel grp / 2, 16-byte
         // chunks 4 (grp % 2) .. 4 (grp % 2) + 3 of the 128-byte row.
         {
-          // dQ(i-2), the last reader of this buffer, completed before drain(i-2).
+          // The last reader of this buffer, dQ(i-2) (one buffer: dQ(i-1)), was
+          // issued before dP^T(i); that product's commit, which this warp waited
+          // for, arrives only after every earlier product has completed.
           const uint32_t rowb =
-              sbase + L::kDS + (L::kDSDouble ? (i & 1) * L::kDSBytes : 0) + (grp >> 1) * L::kPanelBytes;
+              sbase + L::kDS + (L::kDSDouble ? (gi & 1) * L::kDSBytes : 0) + (grp >> 1) * L::kPanelBytes;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             st_shared_v4(rowb + sw128_offset(r, 4 * (grp & 1) + c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
@@ -499,19 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bDSReady));
-        if constexpr (L::kDSDouble) {
-          if (i > 0 && !(ok = drain_dq(i - 1, prv))) break;
-          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 5, i);
-        }
+        cur = nxt;
       }
-      // The loop's last step made prv the cursor of the final tile.
-      if (ok && n_iter > 0) ok = drain_dq(n_iter - 1, prv);
 
-      // ---------------- epilogue: dK (x alpha), dV rows of this key tile ----------------
-      if (ok) ok = wait_warp(bar(L::bMMADone), 0, ctl);
+      // ---------------- item epilogue: dK (x alpha), dV rows of this key tile ----------------
+      // The next item's dV(0) / dK(0), which overwrite these accumulators, wait for
+      // its P^T(0) / dS^T(0), which this warp produces only after this epilogue.
+      if (ok) ok = wait_warp(bar(L::bMMADone), kv & 1, ctl);
       if (ok) {
         tc_fence_after();
-        const size_t row = static_cast<size_t>(bhk) * N + key;
+        const size_t row = static_cast<size_t>(itm.bhk) * N + key;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           const uint32_t col = (which == 0 ? L::kColDK : L::kColDV) + kDG * grp;
@@ -535,15 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }
     }
-    // Every dQ box this warp handed to the TMA unit has completed before the
-    // CTA's shared memory is released.
-    if (L::kTmaDQ) bulk_wait_all_warp();
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
   }
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 32) PFA_BWD_TRACE(0, 32, 0);
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -559,8 +646,12 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = attn_bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  const int n_t = (a.s.N + kTile - 1) / kTile;
-  const dim3 grid(static_cast<unsigned>(n_t) * a.s.B * a.s.Hkv);
+  // Persistent: one CTA per SM (at most one per work item).
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long n_items = static_cast<long long>((a.s.N + kTile - 1) / kTile) * a.s.B * a.s.Hkv;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }

@@ -279,6 +279,17 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Prefetch a 3-D tile into L2 (no shared memory, no completion to wait for);
+// warp-collective like the loads.
+__device__ __forceinline__ void tma_prefetch_l2_3d_warp(const CUtensorMap* m, int x, int y, int z) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // ----------------------------------------------------------------------------
 // tcgen05: TMEM allocation, MMA, commit, loads/stores
 // ----------------------------------------------------------------------------

@@ -57,8 +57,8 @@ cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long 
                          cudaStream_t stream);
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const DeltaAltArgs& a, cudaStream_t stream);
-// tdq: FP32 [B*Hq, N, d] map of the dQ workspace with 16-column x 32-row boxes and
-// 64-byte swizzle (the reduce-add target of the d = 64 kernel).
+// tdq: FP32 [B*Hq, N, d] map of the dQ workspace with 32-column x 32-row boxes and
+// 128-byte swizzle (the reduce-add target of the d = 64 kernel).
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
                        cudaStream_t stream);

@@ -24,7 +24,7 @@
 #define PFA_TRACE_DECL() unsigned int pfa_trace_n_ = 0
 #define PFA_TRACE_EVENT(buf, slot, ev, j)                                                      \
   do {                                                                                         \
-    if (blockIdx.x == 0) {                                                                     \
+    if (blockIdx.x == PFA_TRACE_BLOCK) {                                                       \
       const unsigned long long c_ = clock64();                                                 \
       if (pfa_trace_n_ < 1024)                                                                 \
         buf[slot][pfa_trace_n_] = (static_cast<unsigned long long>(ev) << 56) |                \
