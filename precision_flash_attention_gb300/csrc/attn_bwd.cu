@@ -155,6 +155,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int item0 = static_cast<int>(blockIdx.x);
   const int stride = static_cast<int>(gridDim.x);
+  // The k-th item of this CTA: rounds of gridDim.x items, taken left to right in
+  // even rounds and right to left in odd ones, so that a CTA given a heavy item
+  // early gets a light one in the next round.
+  auto item_at = [&](int k) { return k * stride + ((k & 1) ? stride - 1 - item0 : item0); };
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (L::kTmaDQ) tma_prefetch_desc_warp(&tmdQ);
         int g = 0;        // query tiles issued by this CTA (all items)
         bool ok = true;
-        for (int item = item0; ok && item < n_items; item += stride) {
+        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
           const Item it = decode(item);
           QCursor pc = first_of(it);
           for (int i = 0; i < it.n_iter; ++i, ++g, pc = advance(pc, it)) {
@@ -228,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc_warp(&tmV);
         int kv = 0;
         bool ok = true;
-        for (int item = item0; item < n_items; item += stride) {
+        for (int k = 0, item = item0; item < n_items; ++k, item = item_at(k)) {
           const Item it = decode(item);
           if (kv > 0 && !(ok = wait_warp(bar(L::bKVEmpty), (kv - 1) & 1, ctl))) break;
           mbar_arrive_expect_tx_warp(bar(L::bKVFull), 2 * L::kTileBytes);
@@ -237,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d_warp(sbase + L::kV + p * L::kPanelBytes, &tmV, bar(L::bKVFull), p * 64, it.k0, it.bhk);
           }
           ++kv;
-          if (item + stride < n_items) {
-            const Item nx = decode(item + stride);
+          if (item_at(k + 1) < n_items) {
+            const Item nx = decode(item_at(k + 1));
             for (int p = 0; p < D / 64; ++p) {
               tma_prefetch_l2_3d_warp(&tmK, p * 64, nx.k0, nx.bhk);
               tma_prefetch_l2_3d_warp(&tmV, p * 64, nx.k0, nx.bhk);
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0;
         int kv = 0;
         bool ok = true;
-        for (int item = item0; ok && item < n_items; item += stride, ++kv) {
+        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
           const Item it = decode(item);
           if (!(ok = wait_warp(bar(L::bKVFull), kv & 1, ctl))) break;
           if (!(ok = wait_warp(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl))) break;
@@ -376,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 20) * 8192u;
       bool ok = true;
       int g = 0;
-      for (int item = item0; ok && item < n_items; item += stride) {
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
         const Item itm = decode(item);
         QCursor qc = first_of(itm);
         for (int i = 0; ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
@@ -478,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       int g = 0;   // query tiles of this CTA so far (all items): the barrier phases
-      for (int item = item0, kv = 0; ok && item < n_items; item += stride, ++kv) {
+      for (int k = 0, item = item0, kv = 0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
       const Item itm = decode(item);
       const int k0 = itm.k0;
       const int key = k0 + r;
@@ -487,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gi = g;
         const int q0 = cur.q0;
         // The next query tile: this item's next one or the next item's first.
-        const bool has_nxt = i + 1 < itm.n_iter || item + stride < n_items;
-        const QCursor nxt = i + 1 < itm.n_iter ? advance(cur, itm) : first_of(decode(item + stride));
+        const bool has_nxt = i + 1 < itm.n_iter || item_at(k + 1) < n_items;
+        const QCursor nxt = i + 1 < itm.n_iter ? advance(cur, itm) : first_of(decode(item_at(k + 1)));
         const int slot = gi & 1;
         float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 4 + grp) * 64;
         // Entry rg of this slot was last read two tiles ago; every warp of the

@@ -10,11 +10,16 @@
 // equations, and the fix of paper §4) and the bud-325 note of the same title
 // (Key claims, Method / Algorithm 1).
 //
-// CTA = two 128-row Q tiles (t = 0, 1) of one (batch, query head). 384 threads,
+// A work item is two 128-row Q tiles (t = 0, 1) of one (batch, query head).
+// Persistent: one CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+// heaviest causal pairs first; barrier phases count across items, so setup and
+// teardown happen once per SM and the next item's Q (double buffered for
+// d = 64) and K / V stream in while the current item finishes. 384 threads,
 // one warpgroup per role group (registers are granted per warpgroup):
-//   warp 0      TMA producer (Q0, Q1 once; then K_j and V_j into a stage ring)
-//   warp 1      TMEM owner and single-thread tcgen05.mma issuer
-//   warps 2, 3  idle
+//   warp 0      K / V producer (one ring of stages across items)
+//   warp 1      TMEM owner and tcgen05.mma issuer
+//   warp 2      Q producer (one pair per item)
+//   warp 3      idle
 //   warps 4..7  softmax of tile 0, warps 8..11 softmax of tile 1; one query row
 //               per thread (TMEM lane quarter = warp % 4)
 // TMEM (512 columns): S_t in [128 t, 128 t + 128), O_t in [256 + d t, 256 + d t + d).
@@ -39,14 +44,16 @@ constexpr float kEpsShift = 0.03125f;  // 2^-5
 template <int D>
 struct FwdLayout {
   static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q pairs in flight
   static constexpr int kTileBytes = kTile * D * 2;   // 128 rows x D bf16
   static constexpr int kPanelBytes = kTile * 128;    // 128 rows x 64 bf16
-  static constexpr int kQ = 0;                       // + t * tile
-  static constexpr int kK = 2 * kTileBytes;          // + stage * tile
+  static constexpr int kQ = 0;                       // + (buffer * 2 + t) * tile
+  static constexpr int kK = kQBufs * 2 * kTileBytes; // + stage * tile
   static constexpr int kV = kK + kStages * kTileBytes;
   static constexpr int kBars = kV + kStages * kTileBytes;
-  static constexpr int bQFull = 0;
-  static constexpr int bKVFull = 1;                   // + stage
+  static constexpr int bQFull = 0;                    // + Q buffer
+  static constexpr int bQEmpty = bQFull + kQBufs;     // + Q buffer: the item's products are done
+  static constexpr int bKVFull = bQEmpty + kQBufs;    // + stage
   static constexpr int bKVEmpty = bKVFull + kStages;  // + stage
   static constexpr int bSFull = bKVEmpty + kStages;   // + tile
   static constexpr int bPFull = bSFull + 2;           // + tile
@@ -57,6 +64,7 @@ struct FwdLayout {
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 template <int D, int MODE, bool CAUSAL, bool COUNT>
@@ -78,17 +86,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kt = (N + kTile - 1) / kTile;   // key tiles == query tiles
   const int n_pairs = (n_kt + 1) / 2;
   const int BHq = sh.B * sh.Hq;
-  const int bh = blockIdx.x % BHq;
-  const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x / BHq);  // heaviest first
-  const int b = bh / sh.Hq;
-  const int h = bh % sh.Hq;
-  const int bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
-  const int qt0 = 2 * pair;
-  const bool has1 = qt0 + 1 < n_kt;
-  // Last key tile each query tile visits (-1: the tile does not exist).
-  const int last0 = CAUSAL ? qt0 : n_kt - 1;
-  const int last1 = has1 ? (CAUSAL ? qt0 + 1 : n_kt - 1) : -1;
-  const int n_iter = max(last0, last1) + 1;
+  const int n_items = n_pairs * BHq;
+  const int item0 = static_cast<int>(blockIdx.x);
+  const int stride = static_cast<int>(gridDim.x);
+  // The k-th item of this CTA: rounds of gridDim.x items, taken left to right in
+  // even rounds and right to left in odd ones, so that a CTA given a heavy item
+  // early gets a light one in the next round.
+  auto item_at = [&](int k) { return k * stride + ((k & 1) ? stride - 1 - item0 : item0); };
+  // Work item -> (pair of query tiles, batch and query head); pairs heaviest first.
+  struct Item {
+    int bh, bh_kv, qt0, last0, last1, n_iter;
+    bool has1;
+  };
+  auto decode = [&](int item) {
+    Item it;
+    it.bh = item % BHq;
+    const int pair = n_pairs - 1 - item / BHq;
+    const int b = it.bh / sh.Hq, h = it.bh % sh.Hq;
+    it.bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
+    it.qt0 = 2 * pair;
+    it.has1 = it.qt0 + 1 < n_kt;
+    // Last key tile each query tile visits (-1: the tile does not exist).
+    it.last0 = CAUSAL ? it.qt0 : n_kt - 1;
+    it.last1 = it.has1 ? (CAUSAL ? it.qt0 + 1 : n_kt - 1) : -1;
+    it.n_iter = max(it.last0, it.last1) + 1;
+    return it;
+  };
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -98,7 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
     if (sbase & 1023u) atomicOr(args.err, PFA_DEVERR_SMEM_ALIGN);
-    mbar_init(bar(L::bQFull), 1);
+    for (int qb = 0; qb < L::kQBufs; ++qb) {
+      mbar_init(bar(L::bQFull + qb), 1);
+      mbar_init(bar(L::bQEmpty + qb), 1);
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar(L::bKVFull + s), 1);
       mbar_init(bar(L::bKVEmpty + s), 1);
@@ -121,49 +147,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Register split per warpgroup. The block is launched with 168 registers per
-  // thread (384 x 168 = 64512). Warpgroup 0 (producer, MMA, two idle warps) drops
-  // to 56 and the two softmax warpgroups rise to 224: 128 x 56 + 256 x 224 =
-  // 64512. Each group returns to 168 before the common teardown (the same sum).
+  // thread (384 x 168 = 64512). Warpgroup 0 (producers, MMA, one idle warp)
+  // drops to 64 and the two softmax warpgroups rise to 216: 128 x 64 + 256 x 216
+  // = 63488. Each group returns to 168 before the common teardown.
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
     if (*abort_flag == 0) {
     if (warp == 0) {
-      // ---------------- TMA producer (whole warp, one elected lane issues) ----------------
-      tma_prefetch_desc_warp(&tmQ);
+      // ---------------- K / V producer (whole warp, one elected lane issues) ----------------
+      // One ring of stages for the key tiles of all items of this CTA.
       tma_prefetch_desc_warp(&tmK);
       tma_prefetch_desc_warp(&tmV);
-      mbar_arrive_expect_tx_warp(bar(L::bQFull), (has1 ? 2 : 1) * L::kTileBytes);
-      for (int t = 0; t < (has1 ? 2 : 1); ++t)
-        for (int p = 0; p < D / 64; ++p)
-          tma_load_3d_warp(sbase + L::kQ + t * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                           bar(L::bQFull), p * 64, (qt0 + t) * kTile, bh);
-      int issued = 0;
-      for (int j = 0; j < n_iter; ++j) {
-        const int s = j % L::kStages;
-        const uint32_t ph = (j / L::kStages) & 1;
-        if (!wait_warp(bar(L::bKVEmpty + s), ph ^ 1, ctl)) break;
-        issued = j + 1;
-        mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
-        for (int p = 0; p < D / 64; ++p) {
-          tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
-          tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                           bar(L::bKVFull + s), p * 64, j * kTile, bh_kv);
+      int gk = 0;   // key tiles issued
+      bool ok = true;
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
+        const Item it = decode(item);
+        for (int j = 0; j < it.n_iter; ++j, ++gk) {
+          const int s = gk % L::kStages;
+          if (!(ok = wait_warp(bar(L::bKVEmpty + s), ((gk / L::kStages) & 1) ^ 1, ctl))) break;
+          mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
+          for (int p = 0; p < D / 64; ++p) {
+            tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
+                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
+            tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
+                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
+          }
         }
       }
       // Drain: every issued copy has landed before shared memory is released.
-      wait_drain(bar(L::bQFull), 0, ctl);
-      for (int j = issued > L::kStages ? issued - L::kStages : 0; j < issued; ++j)
+      for (int j = gk > L::kStages ? gk - L::kStages : 0; j < gk; ++j)
         wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
+    } else if (warp == 2) {
+      // ---------------- Q producer: the pair of query tiles of each item ----------------
+      tma_prefetch_desc_warp(&tmQ);
+      int ti = 0;   // items issued
+      bool ok = true;
+      for (int k = 0, item = item0; item < n_items; ++k, item = item_at(k), ++ti) {
+        const Item it = decode(item);
+        const int qb = ti % L::kQBufs;
+        if (!(ok = wait_warp(bar(L::bQEmpty + qb), ((ti / L::kQBufs) & 1) ^ 1, ctl))) break;
+        mbar_arrive_expect_tx_warp(bar(L::bQFull + qb), (it.has1 ? 2 : 1) * L::kTileBytes);
+        for (int t = 0; t < (it.has1 ? 2 : 1); ++t)
+          for (int p = 0; p < D / 64; ++p)
+            tma_load_3d_warp(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + p * L::kPanelBytes, &tmQ,
+                             bar(L::bQFull + qb), p * 64, (it.qt0 + t) * kTile, it.bh);
+        // With one Q buffer the next pair waits for this item: start it into L2.
+        if (L::kQBufs == 1 && item_at(k + 1) < n_items) {
+          const Item nx = decode(item_at(k + 1));
+          for (int t = 0; t < (nx.has1 ? 2 : 1); ++t)
+            for (int p = 0; p < D / 64; ++p) tma_prefetch_l2_3d_warp(&tmQ, p * 64, (nx.qt0 + t) * kTile, nx.bh);
+        }
+      }
+      for (int i = ti > L::kQBufs ? ti - L::kQBufs : 0; i < ti; ++i)
+        wait_drain(bar(L::bQFull + i % L::kQBufs), (i / L::kQBufs) & 1, ctl);
+      (void)ok;
     } else if (warp == 1) {
       // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      auto issue_s = [&](int t, int s) {
+      // S_t = Q_t K_j^T from Q buffer qb and K/V stage s.
+      auto issue_s = [&](int t, int qb, int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          umma_bf16_warp(tmem + 128 * t, sdesc_sw128(sbase + L::kQ + t * L::kTileBytes + koff, 16, 1024),
+          umma_bf16_warp(tmem + 128 * t,
+                         sdesc_sw128(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + koff, 16, 1024),
                          sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
         }
         umma_commit_warp(bar(L::bSFull + t));
@@ -177,41 +225,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             L::kPanelBytes, 1024),
                                 idPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
-      bool ok = wait_warp(bar(L::bQFull), 0, ctl);
-      for (int j = 0; ok && j < n_iter; ++j) {
-        const int s = j % L::kStages;
-        if (!(ok = wait_warp(bar(L::bKVFull + s), (j / L::kStages) & 1, ctl))) break;
-        const bool act0 = j <= last0, act1 = j <= last1;
-        if (lane == 0) PFA_FWD_TRACE(0, 1, j);
-        tc_fence_after();
-        if (act0) issue_s(0, s);
-        if (j > 0 && j - 1 <= last1) {
-          if (!(ok = wait_warp(bar(L::bPFull + 1), (j - 1) & 1, ctl))) break;
-          if (lane == 0) PFA_FWD_TRACE(0, 2, j - 1);
+      // Phases across items: gk key tiles so far (the K/V ring), c_t scores of
+      // tile t so far (SFull_t and PFull_t), ti items (the Q buffers).
+      int gk = 0, c0 = 0, c1 = 0, ti = 0;
+      bool ok = true;
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
+        const Item it = decode(item);
+        const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
+        const int qb = ti % L::kQBufs;
+        if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
+        for (int j = 0; ok && j < n_iter; ++j) {
+          const int s = (gk + j) % L::kStages;
+          if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
+          const bool act0 = j <= last0, act1 = j <= last1;
+          if (lane == 0) PFA_FWD_TRACE(0, 1, j);
           tc_fence_after();
-          const int sp = (j - 1) % L::kStages;
-          issue_pv(1, sp, j - 1);
-          umma_commit_warp(bar(L::bKVEmpty + sp));
-          if (j - 1 == last1) umma_commit_warp(bar(L::bODone + 1));
+          if (act0) issue_s(0, qb, s);
+          if (j > 0 && j - 1 <= last1) {
+            if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + j - 1) & 1, ctl))) break;
+            if (lane == 0) PFA_FWD_TRACE(0, 2, j - 1);
+            tc_fence_after();
+            const int sp = (gk + j - 1) % L::kStages;
+            issue_pv(1, sp, j - 1);
+            umma_commit_warp(bar(L::bKVEmpty + sp));
+            if (j - 1 == last1) umma_commit_warp(bar(L::bODone + 1));
+          }
+          if (act1) issue_s(1, qb, s);
+          if (act0) {
+            if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + j) & 1, ctl))) break;
+            if (lane == 0) PFA_FWD_TRACE(0, 3, j);
+            tc_fence_after();
+            issue_pv(0, s, j);
+            if (j == last0) umma_commit_warp(bar(L::bODone + 0));
+            if (!act1) umma_commit_warp(bar(L::bKVEmpty + s));
+          }
         }
-        if (act1) issue_s(1, s);
-        if (act0) {
-          if (!(ok = wait_warp(bar(L::bPFull + 0), j & 1, ctl))) break;
-          if (lane == 0) PFA_FWD_TRACE(0, 3, j);
-          tc_fence_after();
-          issue_pv(0, s, j);
-          if (j == last0) umma_commit_warp(bar(L::bODone + 0));
-          if (!act1) umma_commit_warp(bar(L::bKVEmpty + s));
+        if (ok && last1 == n_iter - 1) {
+          const int j = n_iter - 1;
+          if ((ok = wait_warp(bar(L::bPFull + 1), (c1 + j) & 1, ctl))) {
+            tc_fence_after();
+            issue_pv(1, (gk + j) % L::kStages, j);
+            umma_commit_warp(bar(L::bKVEmpty + (gk + j) % L::kStages));
+            umma_commit_warp(bar(L::bODone + 1));
+          }
         }
-      }
-      if (ok && last1 == n_iter - 1) {
-        const int j = n_iter - 1;
-        if ((ok = wait_warp(bar(L::bPFull + 1), j & 1, ctl))) {
-          tc_fence_after();
-          issue_pv(1, j % L::kStages, j);
-          umma_commit_warp(bar(L::bKVEmpty + j % L::kStages));
-          umma_commit_warp(bar(L::bODone + 1));
-        }
+        // The item's products are done once this arrives: its Q buffer is free.
+        umma_commit_warp(bar(L::bQEmpty + qb));
+        gk += n_iter;
+        c0 += last0 + 1;
+        c1 += last1 + 1;
       }
       // Drain: no MMA may still read shared memory or write TMEM at teardown.
       umma_commit_warp(bar(L::bDrain));
@@ -226,25 +288,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_drain(bar(L::bRegs), 0, ctl);
     asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::bRegs));
     if (*abort_flag == 0) {
       // ---------------- softmax warps ----------------
       const int t = (warp - 4) >> 2;  // query tile of this warpgroup
-      const int last = t ? last1 : last0;
       const uint32_t quarter = warp & 3;
       const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
-      const int q0 = (qt0 + t) * kTile;
-      const int qrow = q0 + r;
       const uint32_t lane_off = (quarter * 32u) << 16;
       const uint32_t tS = tmem + 128 * t + lane_off;
       const uint32_t tO = tmem + 256 + D * t + lane_off;
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
 
-      float m1 = -INFINITY;                  // running maximum of raw scores
-      bool rep = false;                      // two entries within eps of m1
       // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
       // repeats within eps change their shift.
       auto shift_of = [&](float mx, bool repeated) {
@@ -253,15 +310,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == 1) return r_m > 0.f ? args.beta * r_m : (r_m < 0.f ? 0.f : kEpsShift);
         return r_m + kEpsShift;
       };
+      bool ok = true;
+      int ct = 0, ot = 0;   // phases across items: scores of this tile, items with this tile
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
+      const Item itm = decode(item);
+      const int last = t ? itm.last1 : itm.last0;
+      if (last < 0) continue;             // the pair has no second tile
+      const int bh = itm.bh;
+      const int q0 = (itm.qt0 + t) * kTile;
+      const int qrow = q0 + r;
+      float m1 = -INFINITY;                  // running maximum of raw scores
+      bool rep = false;                      // two entries within eps of m1
       float m_sh = -INFINITY;                // current shift, natural units
       float l0 = 0.f, l1 = 0.f;              // row sum of Pbar (two partial sums)
       int cnt = 0;                           // entries within tau of m1 (raw)
-      bool ok = true;
 
       for (int j = 0; j <= last; ++j) {
         const int k0 = j * kTile;
         const bool need_mask = (CAUSAL && k0 + kTile > q0) || (k0 + kTile > N);
-        if (!(ok = wait_warp(bar(L::bSFull + t), j & 1, ctl))) break;
+        if (!(ok = wait_warp(bar(L::bSFull + t), (ct + j) & 1, ctl))) break;
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 4, j);
         tc_fence_after();
         uint32_t v[128];
@@ -392,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---------------- epilogue ----------------
-      if (ok && last >= 0) ok = wait_warp(bar(L::bODone + t), 0, ctl);
-      if (ok && last >= 0) {
+      if (ok) ok = wait_warp(bar(L::bODone + t), ot & 1, ctl);
+      if (ok) {
         tc_fence_after();
         // The exact final shift; it differs from the one in use only when the last
         // tile's deferred count turned the row repeated. Rescale as a tile would.
@@ -450,6 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      ct += last + 1;
+      ++ot;
+      }
     }
     asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
   }
@@ -470,8 +540,13 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = attn_fwd_kernel<D, MODE, CAUSAL, COUNT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
+  // Persistent: one CTA per SM (at most one per work item).
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int n_kt = (a.s.N + kTile - 1) / kTile;
-  const dim3 grid(static_cast<unsigned>((n_kt + 1) / 2) * a.s.B * a.s.Hq);
+  const long long n_items = static_cast<long long>((n_kt + 1) / 2) * a.s.B * a.s.Hq;
+  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
