@@ -211,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < it.n_iter; ++i, ++g, pc = advance(pc, it)) {
             const int s = g % L::kStages;
             if (!(ok = wait_warp(bar(L::bQEmpty + s), ((g / L::kStages) & 1) ^ 1, ctl))) break;
+            if (lane == 0) PFA_BWD_TRACE(4, 40, g);
             mbar_arrive_expect_tx_warp(bar(L::bQFull + s), 2 * L::kTileBytes);
             for (int p = 0; p < D / 64; ++p) {
               tma_load_3d_warp(sbase + L::kQ + s * L::kTileBytes + p * L::kPanelBytes, &tmQ,
@@ -251,6 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kv > 0) wait_drain(bar(L::bKVFull), (kv - 1) & 1, ctl);
         (void)ok;
+#if defined(PFA_TRACE) && defined(PFA_TRACE_QOBS)
+      } else if (warp == 3) {
+        // Trace builds only: time at which each query stage of the first item lands.
+        const Item it0 = decode(item0);
+        for (int g = 0; g < it0.n_iter && g < 1000; ++g) {
+          if (!wait_drain(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl)) break;
+          if (lane == 0) PFA_BWD_TRACE(6, 42, g);
+        }
+#endif
       } else if (warp == 1) {
         // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
         // Order per query tile i: dV(i), S^T(i+1), dK(i), then dP^T(i+1) and dQ(i)
@@ -311,6 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kTile / 16; ++kk)
               umma_bf16_tmem_a_warp(tDV, tS + packed_col(kk), sdesc_sw128(sDO + kk * 2048, L::kPanelBytes, 1024),
                                     idKM, (i > 0 || kk > 0) ? 1u : 0u);
+            if (lane == 0) PFA_BWD_TRACE(0, 43, gg);
             if (more) {
               const int s1 = (gg + 1) % L::kStages;
               if (!(ok = wait_warp(bar(L::bQFull + s1), ((gg + 1) / L::kStages) & 1, ctl))) break;
@@ -326,13 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kTile / 16; ++kk)
               umma_bf16_tmem_a_warp(tDK, tDP + packed_col(kk), sdesc_sw128(sQ + kk * 2048, L::kPanelBytes, 1024),
                                     idKM, (i > 0 || kk > 0) ? 1u : 0u);
+            if (lane == 0) PFA_BWD_TRACE(0, 44, gg);
             // dK(i) is the last reader of this Q / dO stage (dQ reads dS and K).
             umma_commit_warp(bar(L::bQEmpty + s));
             if constexpr (L::kDSDouble) {
               // dP^T(i+1) overwrites dS^T(i) after dK(i) has read it; dQ(i) reads its
               // own dS buffer and waits only until dQ(i-1) has left TMEM.
               if (more) issue_dp(gg + 1);
+              if (lane == 0) PFA_BWD_TRACE(0, 45, gg);
               if (gg > 0 && !(ok = wait_warp(bar(L::bDQFree), (gg - 1) & 1, ctl))) break;
+              if (lane == 0) PFA_BWD_TRACE(0, 46, gg);
             }
             tc_fence_after();
             const uint32_t sDS = sbase + L::kDS + (L::kDSDouble ? (gg & 1) * L::kDSBytes : 0);
@@ -340,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < kTile / 16; ++kk)
               umma_bf16_warp(tDQ, sdesc_sw128(sDS + kk * 2048, L::kPanelBytes, 1024),
                              sdesc_sw128(sbase + L::kK + kk * 2048, L::kPanelBytes, 1024), idMM, kk > 0);
+            if (lane == 0) PFA_BWD_TRACE(0, 47, gg);
             umma_commit_warp(bar(L::bDQFull));
             if constexpr (!L::kDSDouble) {
               if (more) {
@@ -386,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
         const int it = g;
         if (!(ok = wait_warp(bar(L::bDQFull), it & 1, ctl))) break;
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(3, 13, it);
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 13, it);
         tc_fence_after();
         if constexpr (L::kTmaDQ) {
           // Two 32 x 32 FP32 boxes (128-byte swizzle) per warp; the previous
@@ -415,6 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int y = qc.q0 + 32 * static_cast<int>(quarter);
           tma_reduce_add_3d_warp(&tmdQ, dq_stage, 0, y, qc.bh);
           tma_reduce_add_3d_warp(&tmdQ, dq_stage + 4096u, 32, y, qc.bh);
+          if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 41, it);
         } else {
           const int q = qc.q0 + static_cast<int>(quarter) * 32 + lane;
           float* dq_row = args.dq_accum + (static_cast<size_t>(qc.bh) * N + q) * D;
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(3, 5, it);
+        if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 5, it);
         }
       }
     }

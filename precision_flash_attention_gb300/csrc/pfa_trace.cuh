@@ -10,9 +10,9 @@
 
 #ifdef PFA_TRACE
 // The buffer comes with a host reader `<name>_read(out, clear)`: clear != 0
-// zeroes the buffer, otherwise its 4 x 1024 words are copied to `out`.
+// zeroes the buffer, otherwise its 8 x 1024 words are copied to `out`.
 #define PFA_TRACE_BUFFER(name)                                                                \
-  __device__ unsigned long long name[4][1024];                                                 \
+  __device__ unsigned long long name[8][1024];                                                 \
   extern "C" int name##_read(unsigned long long* out, int clear) {                             \
     void* p_ = nullptr;                                                                        \
     cudaDeviceSynchronize();                                                                   \
