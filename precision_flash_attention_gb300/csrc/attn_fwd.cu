@@ -23,10 +23,14 @@
 //   warps 4..7  softmax of tile 0, warps 8..11 softmax of tile 1; one query row
 //               per thread (TMEM lane quarter = warp % 4)
 // TMEM (512 columns): S_t in [128 t, 128 t + 128), O_t in [256 + d t, 256 + d t + d).
-// Pbar_t (BF16) is written over the first 64 columns of S_t and is the TMEM A
-// operand of Obar_t += Pbar_t V.
-// The tensor core runs S0_j, PV1_{j-1}, S1_j, PV0_j, ... so that each tile's
-// softmax overlaps the other tile's two products.
+// Pbar_t (BF16) is the TMEM A operand of Obar_t += Pbar_t V. At d = 64 it has
+// its own columns [384 + 64 t, 448 + 64 t): once the softmax has read S_t(j)
+// into registers the tensor core computes S_t(j+1), so each softmax warpgroup
+// finds its next scores ready when it finishes a tile; the tensor core runs
+// S0_j, S1_j, PV0_{j-1}, PV1_{j-1}, ... At d = 128 (no columns left) Pbar_t is
+// written over the first 64 columns of S_t and the tensor core runs S0_j,
+// PV1_{j-1}, S1_j, PV0_j, ... so that each tile's softmax overlaps the other
+// tile's two products.
 #include "pfa_device.cuh"
 #include "pfa_trace.cuh"
 
@@ -45,6 +49,11 @@ template <int D>
 struct FwdLayout {
   static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q pairs in flight
+  // d = 64: Pbar_t gets its own TMEM columns [384 + 64 t, 448 + 64 t), so the
+  // next S_t can be computed as soon as the softmax holds the current one in
+  // registers. d = 128 has no columns left and writes Pbar_t over S_t.
+  static constexpr bool kSplitP = (D == 64);
+  static constexpr uint32_t kColP = 384;
   static constexpr int kTileBytes = kTile * D * 2;   // 128 rows x D bf16
   static constexpr int kPanelBytes = kTile * 128;    // 128 rows x 64 bf16
   static constexpr int kQ = 0;                       // + (buffer * 2 + t) * tile
@@ -58,7 +67,9 @@ struct FwdLayout {
   static constexpr int bSFull = bKVEmpty + kStages;   // + tile
   static constexpr int bPFull = bSFull + 2;           // + tile
   static constexpr int bODone = bPFull + 2;           // + tile
-  static constexpr int bDrain = bODone + 2;
+  static constexpr int bSFree = bODone + 2;           // + tile: the softmax holds S_t (split Pbar)
+  static constexpr int bPVDone = bSFree + 2;          // + tile: Obar_t += Pbar_t V done (split Pbar)
+  static constexpr int bDrain = bPVDone + 2;
   static constexpr int bRegs = bDrain + 1;          // the softmax warps hold their registers
   static constexpr int kNumBars = bRegs + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
@@ -133,6 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bSFull + t), 1);
       mbar_init(bar(L::bPFull + t), 4);
       mbar_init(bar(L::bODone + t), 1);
+      mbar_init(bar(L::bSFree + t), 4);
+      mbar_init(bar(L::bPVDone + t), 1);
     }
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bRegs), 8);
@@ -216,11 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit_warp(bar(L::bSFull + t));
       };
-      // Obar_t (+)= Pbar_t V_j; Pbar_t is columns [0, 64) of S_t, 8 columns per K step.
+      // Obar_t (+)= Pbar_t V_j; Pbar_t is 64 BF16-pair columns (its own with the
+      // split layout, else the first 64 of S_t), 8 columns per K step.
       auto issue_pv = [&](int t, int s, int j) {
+        const uint32_t tp = tmem + (L::kSplitP ? L::kColP + 64u * t : 128u * t);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_tmem_a_warp(tmem + 256 + D * t, tmem + 128 * t + 8 * kk,
+          umma_bf16_tmem_a_warp(tmem + 256 + D * t, tp + 8 * kk,
                                 sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
                                             L::kPanelBytes, 1024),
                                 idPV, (j > 0 || kk > 0) ? 1u : 0u);
@@ -229,6 +244,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       // tile t so far (SFull_t and PFull_t), ti items (the Q buffers).
       int gk = 0, c0 = 0, c1 = 0, ti = 0;
       bool ok = true;
+      if constexpr (L::kSplitP) {
+        // Split Pbar: per key tile j, S_0(j) and S_1(j) (each once its softmax
+        // holds the previous scores of its tile), then the products of key tile
+        // j - 1 with each tile's Pbar. The scores of the next key tile are thus
+        // computed while the softmax works on the current one.
+        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
+          const Item it = decode(item);
+          const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
+          const int qb = ti % L::kQBufs;
+          if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
+          for (int j = 0; ok && j <= n_iter; ++j) {
+            if (j < n_iter) {
+              const int s = (gk + j) % L::kStages;
+              if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
+              if (lane == 0) PFA_FWD_TRACE(0, 1, j);
+              if (j <= last0) {
+                if (c0 + j > 0 && !(ok = wait_warp(bar(L::bSFree + 0), (c0 + j - 1) & 1, ctl))) break;
+                tc_fence_after();
+                issue_s(0, qb, s);
+              }
+              if (j <= last1) {
+                if (c1 + j > 0 && !(ok = wait_warp(bar(L::bSFree + 1), (c1 + j - 1) & 1, ctl))) break;
+                tc_fence_after();
+                issue_s(1, qb, s);
+              }
+            }
+            if (j > 0) {
+              const int jp = j - 1;
+              const int sp = (gk + jp) % L::kStages;
+              if (jp <= last0) {
+                if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + jp) & 1, ctl))) break;
+                if (lane == 0) PFA_FWD_TRACE(0, 3, jp);
+                tc_fence_after();
+                issue_pv(0, sp, jp);
+                umma_commit_warp(bar(L::bPVDone + 0));
+                if (jp == last0) umma_commit_warp(bar(L::bODone + 0));
+              }
+              if (jp <= last1) {
+                if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + jp) & 1, ctl))) break;
+                if (lane == 0) PFA_FWD_TRACE(0, 2, jp);
+                tc_fence_after();
+                issue_pv(1, sp, jp);
+                umma_commit_warp(bar(L::bPVDone + 1));
+                if (jp == last1) umma_commit_warp(bar(L::bODone + 1));
+              }
+              umma_commit_warp(bar(L::bKVEmpty + sp));
+            }
+          }
+          // The item's products are done once this arrives: its Q buffer is free.
+          umma_commit_warp(bar(L::bQEmpty + qb));
+          gk += n_iter;
+          c0 += last0 + 1;
+          c1 += last1 + 1;
+        }
+      } else {
       for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
         const Item it = decode(item);
         const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
@@ -275,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         c0 += last0 + 1;
         c1 += last1 + 1;
       }
+      }
       // Drain: no MMA may still read shared memory or write TMEM at teardown.
       umma_commit_warp(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, ctl);
@@ -299,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_off = (quarter * 32u) << 16;
       const uint32_t tS = tmem + 128 * t + lane_off;
       const uint32_t tO = tmem + 256 + D * t + lane_off;
+      const uint32_t tP = L::kSplitP ? tmem + L::kColP + 64 * t + lane_off : tS;   // Pbar_t
       const float sl2 = sh.scale_log2;
       const float alpha = sh.scale;
 
@@ -336,6 +408,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld64(tS + 64, v + 64);
         tmem_ld_wait64(v);
         tmem_ld_wait64(v + 64);
+        if constexpr (L::kSplitP) {
+          // The scores are in registers: the next S_t may overwrite them.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::bSFree + t));
+        }
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < kTile; ++c) {
@@ -360,19 +438,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         //                        entries >= t1 - eps;
         //   m1 - eps <= t1 <= m1: repeated (an entry of this tile ties the maximum);
         //   otherwise the flag is unchanged.
-        // The count of a tile whose maximum jumped by more than eps is taken after
-        // this tile's Pbar has been handed over (below), so this tile's shift uses
-        // "not repeated" for such a row and the next tile's shift the exact flag.
-        // An intermediate shift only changes this tile's BF16 rounding: Obar and l
-        // are rescaled whenever the shift moves, and the epilogue applies the
-        // exact final shift.
+        // Two entries of the tile reach a threshold iff two of the eight 16-column
+        // blocks do or two of the sixteen column classes (column mod 16) do: a
+        // single qualifying entry lies in one block and one class, and two
+        // distinct entries differ in their block or in their class. So the block
+        // maxima and the class maxima settle it without a data-dependent scan.
         bool jump = false;
-        float thr_eps = 0.f;
         if (kTies) {
-          thr_eps = t1 - args.eps_raw;
+          const float thr_eps = t1 - args.eps_raw;
           jump = t1 > m1 && m1 < thr_eps;
+          bool two = false;
+          if (__any_sync(0xFFFFFFFFu, jump)) {
+            int nb = 0, ne = 0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              auto x = [&](int k) { return __uint_as_float(v[16 * k + e]); };
+              const float ce = fmaxf(fmax3(x(0), x(1), x(2)), fmax3(x(3), fmax3(x(4), x(5), x(6)), x(7)));
+              ne += ce >= thr_eps ? 1 : 0;
+            }
+            two = nb >= 2 || ne >= 2;
+          }
           if (t1 > m1) {
-            rep = !jump;
+            rep = jump ? two : true;
           } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
             rep = true;
           }
@@ -383,13 +472,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const float m_new = shift_of(m1, rep);
         const bool changed = (j > 0) && (m_new != m_sh);
+        if constexpr (L::kSplitP) {
+          // Obar_t and the Pbar_t columns are free once the previous key tile's
+          // product has completed (tile 0 of an item: its epilogue waited for
+          // the last product of the previous item).
+          // A failed wait ends the loop at the bottom of this iteration: a break
+          // here, with all the scores live, defeats register allocation.
+          if (j > 0) {
+            ok = wait_warp(bar(L::bPVDone + t), (ct + j - 1) & 1, ctl);
+            tc_fence_after();
+          }
+        }
         const float corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
         l0 *= corr;
         l1 *= corr;
         m_sh = m_new;
 
-        // Rescale Obar where the shift moved. S_t of this tile was committed after
-        // the previous P.V of this tile, so that product has completed.
+        // Rescale Obar where the shift moved. The previous P.V of this tile has
+        // completed: split Pbar waited for it above, otherwise S_t of this tile
+        // was committed after it.
         if (__any_sync(0xFFFFFFFFu, changed)) {
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
@@ -426,48 +527,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             add2(l0, l1, p0, p1);
             pk[u] = pack_bf16x2(p0, p1);
           }
-          tmem_st32(tS + 32 * half, pk);
+          tmem_st32(tP + 32 * half, pk);
         }
         if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
         tmem_st_wait();
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 7, j);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+        if (lane == 0 && ok) mbar_arrive(bar(L::bPFull + t));
 
-        // The deferred count: rows whose maximum jumped are repeated iff two of
-        // this tile's entries reach t1 - eps. Two blocks at or above it settle it;
-        // otherwise only the one block holding t1 is counted.
-        if (kTies && __any_sync(0xFFFFFFFFu, jump)) {
-          int nb = 0;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
-          bool r2 = nb >= 2;
-          const bool scan = jump && nb < 2;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const bool mine = scan && bm[k] >= thr_eps;
-            if (__any_sync(0xFFFFFFFFu, mine)) {
-              int c = 0;
-#pragma unroll
-              for (int e = 0; e < 16; ++e) c += __uint_as_float(v[16 * k + e]) >= thr_eps ? 1 : 0;
-              if (mine) r2 = c >= 2;
-            }
-          }
-          if (jump) rep = r2;
-        }
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 8, j);
+        if (!ok) break;
       }
 
       // ---------------- epilogue ----------------
       if (ok) ok = wait_warp(bar(L::bODone + t), ot & 1, ctl);
       if (ok) {
         tc_fence_after();
-        // The exact final shift; it differs from the one in use only when the last
-        // tile's deferred count turned the row repeated. Rescale as a tile would.
-        const float m_fin = shift_of(m1, rep);
-        const float fcorr = (MODE > 0 && m_fin != m_sh) ? ex2_approx((m_sh - m_fin) * kLog2e) : 1.f;
-        l0 *= fcorr;
-        l1 *= fcorr;
+        // The flag is exact after every tile, so the shift in use is the final one.
+        const float m_fin = m_sh;
         const float l = l0 + l1;
         const bool row_ok = qrow < N;
         const float inv_l = 1.f / l;
@@ -482,7 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             float y0 = __uint_as_float(o[2 * u]), y1 = __uint_as_float(o[2 * u + 1]);
-            if (MODE > 0) mul2(y0, y1, fcorr);
             mul2(y0, y1, inv_l);
             pk[u] = pack_bf16x2(y0, y1);
           }
