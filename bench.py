@@ -174,8 +174,8 @@ class ClockSampler:
 
 
 def traffic_for(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    sources (null otherwise)."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the kernel's
+    current sources (null otherwise)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -184,7 +184,7 @@ def traffic_for(kernel: str):
         with open(p, encoding="utf-8") as f:
             j = json.load(f)
         e = j.get(kernel)
-        if not e or e.get("source_digest") != _b.source_digest():
+        if not e or e.get("source_digest") != _b.kernel_source_digest(kernel):
             return None
         return e.get("dram_bytes_per_launch_full_workload")
     except (OSError, ValueError, KeyError):
@@ -197,7 +197,8 @@ _SI = {"byte": 1.0, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
 def write_traffic(csv_path: str, kernel: str, command: str) -> dict:
     """Average DRAM bytes (read + write) per launch of `kernel` from an ncu --csv capture
     of dram__bytes_read.sum and dram__bytes_write.sum, stored in profiles/traffic.json
-    under the digest of the current sources (so a later kernel change reads as null)."""
+    under the digest of the kernel's current sources (so a later change to them reads as
+    null)."""
     import csv
     from precision_flash_attention_gb300 import build as _b
     per_launch = {}
@@ -219,7 +220,7 @@ def write_traffic(csv_path: str, kernel: str, command: str) -> dict:
         with open(p, encoding="utf-8") as f:
             data = json.load(f)
     data[kernel] = {"dram_bytes_per_launch_full_workload": sum(per_launch.values()) / len(per_launch),
-                    "launches": len(per_launch), "source_digest": _b.source_digest(),
+                    "launches": len(per_launch), "source_digest": _b.kernel_source_digest(kernel),
                     "workload": dict(WORKLOAD), "command": command}
     with open(p, "w", encoding="utf-8") as f:
         json.dump(data, f, indent=1, sort_keys=True)

@@ -46,6 +46,23 @@ def source_digest() -> str:
     return h.hexdigest()
 
 
+# The translation unit of each kernel; its traffic record is keyed to that file,
+# the API file that builds its launch arguments and the shared headers.
+KERNEL_SOURCES = {"attn_bwd_kernel": "attn_bwd.cu", "convert_dq_kernel": "attn_bwd.cu",
+                  "attn_fwd_kernel": "attn_fwd.cu", "delta_kernel": "attn_delta.cu",
+                  "delta_alt_kernel": "attn_delta.cu"}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    """Hash of the sources one kernel is built from (see KERNEL_SOURCES)."""
+    h = hashlib.sha256()
+    tus = [KERNEL_SOURCES[kernel], "attn_api.cu"]
+    for path in [os.path.join(CSRC, s) for s in tus] + HEADERS + [os.path.join(CSRC, "pfa_trace.cuh")]:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def _digest() -> str:
     h = hashlib.sha256()
     h.update(platform.machine().encode())
