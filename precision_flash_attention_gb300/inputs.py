@@ -128,6 +128,43 @@ def integer_grid(B, H_q, H_kv, N, d, *, causal=False, n_planted=8, seed=0) -> di
             "v": v.to(torch.bfloat16).contiguous(), "do": do.to(torch.bfloat16).contiguous()}
 
 
+# Planted score patterns over two 128-key tiles (raw scores K / 8 for one-hot
+# queries). Each entry: (keys of tile 0 set to a value, keys of tile 1 set to a
+# value); every other key stays at or below 4 (score <= 0.5).
+TIE_PATTERNS = {
+    "jump_same_block": ({10: 8.0}, {128 + 3: 16.0, 128 + 5: 15.875}),
+    "jump_same_class": ({10: 8.0}, {128 + 3: 16.0, 128 + 19: 15.875}),
+    "jump_block_and_class": ({10: 8.0}, {128 + 3: 16.0, 128 + 40: 15.875}),
+    "jump_single": ({10: 8.0}, {128 + 3: 16.0}),
+    "jump_near_miss": ({10: 8.0}, {128 + 3: 16.0, 128 + 5: 15.5}),
+    "jump_exact_pair": ({10: 8.0}, {128 + 3: 16.0, 128 + 4: 16.0}),
+    "tie_below_running_max": ({10: 16.0}, {128 + 7: 15.875}),
+    "rise_within_eps": ({10: 15.875}, {128 + 7: 16.0}),
+}
+
+
+def tie_patterns(names, N=256, d=64, *, seed=0) -> dict:
+    """B=1, H=1 input whose query row i has the key scores of pattern names[i % len(names)]
+    (TIE_PATTERNS): query i is one-hot on feature i % len(names), and feature f of the
+    keys holds pattern f. Background keys are integers in [-16, 4]; V, dO ~ N(0, 1).
+    With scale 1/8 the planted scores are 1.0, 2.0, 2.0 - 2^-6 and 2.0 - 2^-4, exact in
+    BF16, FP32 and FP64."""
+    assert N >= 256 and d >= len(names)
+    g = _gen(seed)
+    q = torch.zeros(1, 1, N, d)
+    for i in range(N):
+        q[0, 0, i, i % len(names)] = 1.0
+    k = torch.randint(-16, 5, (1, 1, N, d), generator=g).to(torch.float32)
+    for f, name in enumerate(names):
+        t0, t1 = TIE_PATTERNS[name]
+        for j, x in list(t0.items()) + list(t1.items()):
+            k[0, 0, j, f] = x
+    v = _normal((1, 1, N, d), 1.0, g)
+    do = _normal((1, 1, N, d), 1.0, g)
+    return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
+            "v": v.to(torch.bfloat16).contiguous(), "do": do.to(torch.bfloat16).contiguous()}
+
+
 def sink_heavy(B=4, H=12, N=2048, d=64, *, seed=0, dup_frac=0.10) -> dict:
     """The sink-heavy stress input (scale 1/8).
 

@@ -233,3 +233,19 @@ def test_unconditional_beta_shift_is_rejected_variant():
     assert l[0] == 0.0
     m_ok = oracle.fix_shift(r_m, np.array([False]), 1, 2.0, True)
     assert oracle.ftz32(np.exp(oracle.fp32(s - m_ok[:, None]))).sum(1)[0] > 0
+
+
+# Planted tie patterns (inputs.TIE_PATTERNS): the flag each construction fixes by
+# definition (two scores within eps = 0.05 of the row maximum, scale 1/8).
+TIE_LABELS = {"jump_same_block": True, "jump_same_class": True, "jump_block_and_class": True,
+              "jump_single": False, "jump_near_miss": False, "jump_exact_pair": True,
+              "tie_below_running_max": True, "rise_within_eps": True}
+
+
+@pytest.mark.parametrize("name", sorted(TIE_LABELS))
+def test_planted_tie_patterns(name):
+    t = inputs.tie_patterns([name])
+    q, k, v = (t[n].double().numpy() for n in ("q", "k", "v"))
+    r = oracle.attn_fwd(q, k, v, causal=False, scale=0.125, fix_mode=1, beta=2.0, eps=0.05)
+    assert r["repeated"].all() if TIE_LABELS[name] else not r["repeated"].any()
+    assert r["counters"]["repeated_rows"] == (256 if TIE_LABELS[name] else 0)

@@ -73,6 +73,39 @@ def test_grid_counters_bit_exact(mode, causal, shape):
                                  names=("dq",))
 
 
+# ---------------------------------------------------------------- planted tie patterns
+# The flag each construction fixes by definition (inputs.TIE_PATTERNS, eps = 0.05 in
+# scaled units, scale 1/8): the repeated-maximum test in the jump tile must see a second
+# entry in the same 16-column block, in the same column class, in neither, or none.
+TIE_LABELS = {"jump_same_block": True, "jump_same_class": True, "jump_block_and_class": True,
+              "jump_single": False, "jump_near_miss": False, "jump_exact_pair": True,
+              "tie_below_running_max": True, "rise_within_eps": True}
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("name", sorted(TIE_LABELS))
+def test_planted_tie_patterns(name, mode):
+    t = inputs.tie_patterns([name])
+    got = run_gpu(t, causal=False, scale=0.125, fix_mode=mode, beta=2.0, eps=0.05, bwd=False)
+    ref = oracle_full(t, causal=False, scale=0.125, fix_mode=mode, beta=2.0, eps=0.05, bwd=False)
+    assert ref["counters"]["repeated_rows"] == (256 if TIE_LABELS[name] else 0)
+    assert got["counters"] == ref["counters"]
+    assert_fwd_close(got, ref, name)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_planted_tie_patterns_mixed(mode):
+    # All eight patterns interleaved row by row: each warp holds rows that jump and rows
+    # that do not, and rows whose second entry sits in different places.
+    names = sorted(TIE_LABELS)
+    t = inputs.tie_patterns(names, N=512)
+    got = run_gpu(t, causal=False, scale=0.125, fix_mode=mode, beta=2.0, eps=0.05, bwd=False)
+    ref = oracle_full(t, causal=False, scale=0.125, fix_mode=mode, beta=2.0, eps=0.05, bwd=False)
+    assert ref["counters"]["repeated_rows"] == 512 * sum(TIE_LABELS.values()) // len(names)
+    assert got["counters"] == ref["counters"]
+    assert_fwd_close(got, ref, "mixed")
+
+
 # ---------------------------------------------------------------- ragged shapes
 RAGGED = [
     # B, Hq, Hkv, N, d, causal
