@@ -53,13 +53,35 @@ KERNEL_SOURCES = {"attn_bwd_kernel": "attn_bwd.cu", "convert_dq_kernel": "attn_b
                   "delta_alt_kernel": "attn_delta.cu"}
 
 
+def _product_text(path: str) -> bytes:
+    """A source file without what only trace builds (-DPFA_TRACE) compile: lines that
+    invoke a trace macro and `#if defined(PFA_TRACE) ...` blocks."""
+    out, depth = [], 0
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            t = line.strip()
+            if depth:
+                if t.startswith("#if"):
+                    depth += 1
+                elif t.startswith("#endif"):
+                    depth -= 1
+                continue
+            if t.startswith("#if defined(PFA_TRACE)"):
+                depth = 1
+                continue
+            if "_TRACE(" in t and "define" not in t:
+                continue
+            out.append(line)
+    return "".join(out).encode()
+
+
 def kernel_source_digest(kernel: str) -> str:
-    """Hash of the sources one kernel is built from (see KERNEL_SOURCES)."""
+    """Hash of the sources one kernel is built from (see KERNEL_SOURCES), as the
+    product build compiles them."""
     h = hashlib.sha256()
     tus = [KERNEL_SOURCES[kernel], "attn_api.cu"]
-    for path in [os.path.join(CSRC, s) for s in tus] + HEADERS + [os.path.join(CSRC, "pfa_trace.cuh")]:
-        with open(path, "rb") as f:
-            h.update(f.read())
+    for path in [os.path.join(CSRC, s) for s in tus] + HEADERS:
+        h.update(_product_text(path))
     return h.hexdigest()
 
 

@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
           const Item it = decode(item);
           if (!(ok = wait_warp(bar(L::bKVFull), kv & 1, ctl))) break;
+          if (lane == 0) PFA_BWD_TRACE(0, 37, kv);
           if (!(ok = wait_warp(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl))) break;
           // With dQ over the dP^T columns (d = 128), dP^T(0) waits until the
           // previous item's last dQ has been drained.
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Two 32 x 32 FP32 boxes (128-byte swizzle) per warp; the previous
           // tile's boxes have been read out before they are rewritten.
           bulk_wait_read_warp();
+          if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 35, it);
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t v[32];
@@ -416,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_before();
               __syncwarp();
               if (lane == 0) mbar_arrive(bar(L::bDQFree));
+              if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 36, it);
             }
             const uint32_t box = dq_stage + 4096u * c;
 #pragma unroll
@@ -513,9 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* stage = reinterpret_cast<float*>(smem + L::kLse) + (slot * 4 + grp) * 64;
         // Entry rg of this slot was last read two tiles ago; every warp of the
         // group has passed the previous tile's wait since, so no one still reads it.
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 26, i);
         if (rg < 64) stage[rg] = rg < 32 ? (pre_in ? -pre * kLog2e : -INFINITY) : (pre_in ? -pre : 0.f);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bLse + 2 * grp + slot));
+        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 27, i);
         if (!(ok = wait_warp(bar(L::bLse + 2 * grp + slot), (gi >> 1) & 1, ctl))) break;
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 4, i);
 
@@ -617,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next item's dV(0) / dK(0), which overwrite these accumulators, wait for
       // its P^T(0) / dS^T(0), which this warp produces only after this epilogue.
       if (ok) ok = wait_warp(bar(L::bMMADone), kv & 1, ctl);
+      if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 25, kv);
       if (ok) {
         tc_fence_after();
         const size_t row = static_cast<size_t>(itm.bhk) * N + key;
@@ -631,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t v[16];
             tmem_ld16(tmem + col + lane_off + c, v);
             tmem_ld_wait16(v);
+            if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 33 + which, kv);
             if (key < N) {
               uint4* dst = reinterpret_cast<uint4*>(out + c);
 #pragma unroll
