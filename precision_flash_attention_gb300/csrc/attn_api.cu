@@ -82,12 +82,12 @@ int check_sizes(int B, int Hq, int Hkv, int N, int d) {
 bool good_scale(float s) { return std::isfinite(s) && s > 0.f; }
 
 // [B*H, N, d] BF16 tensor, boxes of 64 columns (128 bytes, 128B swizzle) x 128 rows.
-int tile_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+int tile_map(CUtensorMap* m, const void* base, int BH, int N, int d, int rows = pfa::kTile) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pfa::kTile), 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -234,8 +234,11 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
-  CUtensorMap tdq;
+  CUtensorMap tdq, tdk, tdv;
   if ((rc = f32_box_map(&tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
+  // dK, dV leave through 64-column x 32-row boxes (d = 64: one drain warp's rows).
+  if ((rc = tile_map(&tdk, dk, B * H_kv, N, d, 32)) != PFA_OK) return rc;
+  if ((rc = tile_map(&tdv, dv, B * H_kv, N, d, 32)) != PFA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
   if ((rc = launched(cudaMemsetAsync(dq_accum, 0, ws, st))) != PFA_OK) return rc;
@@ -248,7 +251,7 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   a.dv = dv;
   a.err = dev->err;
   a.err_site = dev->site;
-  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, tdq, a, st))) != PFA_OK) return rc;
+  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, st))) != PFA_OK) return rc;
   return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
 }
 

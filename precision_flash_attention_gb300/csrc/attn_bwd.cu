@@ -88,7 +88,8 @@ struct BwdLayout {
   static constexpr int bMMADone = bLse + 8;        // the item's products are done (dK, dV final)
   static constexpr int bDrain = bMMADone + 1;
   static constexpr int bRegs = bDrain + 1;          // the compute warps hold their registers
-  static constexpr int kNumBars = bRegs + 1;
+  static constexpr int bEpiDone = bRegs + 1;        // the drain warps have read the item's dK, dV
+  static constexpr int kNumBars = bEpiDone + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
@@ -104,7 +105,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const __grid_constant__ CUtensorMap tmdQ, const BwdArgs args) {
+                    const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
+                    const __grid_constant__ CUtensorMap tmdV, const BwdArgs args) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(L::bMMADone), 1);
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bRegs), 20);
+    mbar_init(bar(L::bEpiDone), 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -202,7 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One stream of query tiles across all items of this CTA.
         tma_prefetch_desc_warp(&tmQ);
         tma_prefetch_desc_warp(&tmdO);
-        if (L::kTmaDQ) tma_prefetch_desc_warp(&tmdQ);
+        if (L::kTmaDQ) {
+          tma_prefetch_desc_warp(&tmdQ);
+          tma_prefetch_desc_warp(&tmdK);
+          tma_prefetch_desc_warp(&tmdV);
+        }
         int g = 0;        // query tiles issued by this CTA (all items)
         bool ok = true;
         for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
@@ -317,6 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dV += P^T dO : A = P^T in TMEM (keys x queries), B = dO as [d x queries].
             if (!(ok = wait_warp(bar(L::bPReady), gg & 1, ctl))) break;
             if (lane == 0) PFA_BWD_TRACE(0, 2, gg);
+            // dV(0) and dK(0) overwrite the accumulators: with the drain warps
+            // storing dK / dV (d = 64) they wait until the previous item's are read.
+            if (L::kTmaDQ && i == 0 && kv > 0 && !(ok = wait_warp(bar(L::bEpiDone), (kv - 1) & 1, ctl)))
+              break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
@@ -396,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dq_stage = sbase + L::kDQStage + static_cast<uint32_t>(warp - 20) * 8192u;
       bool ok = true;
       int g = 0;
+      int kv = 0;   // items drained (the MMADone phases)
       for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
         const Item itm = decode(item);
         QCursor qc = first_of(itm);
@@ -457,6 +469,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 5, it);
+        }
+        if constexpr (L::kTmaDQ) {
+          // ---------------- item epilogue: alpha dK and dV of this key tile ----------------
+          // This warp's 32 key rows of dK then dV become two BF16 64-column boxes
+          // in its staging area, stored by TMA: the compute warps go straight on
+          // to the next item, and the stores leave asynchronously.
+          if (ok) ok = wait_warp(bar(L::bMMADone), kv & 1, ctl);
+          if (ok) {
+            tc_fence_after();
+            bulk_wait_read_warp();   // the staging area's last dQ boxes have been read
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+              const uint32_t col = which == 0 ? L::kColDK : L::kColDV;
+              const float sc = which == 0 ? alpha : 1.f;
+              const uint32_t box = dq_stage + 4096u * static_cast<uint32_t>(which);
+#pragma unroll 1
+              for (int c = 0; c < 2; ++c) {   // columns 32 c .. 32 c + 31
+                uint32_t v[32];
+                tmem_ld32(tmem + col + lane_off + 32 * c, v);
+                tmem_ld_wait32(v);
+                if (which == 1 && c == 1) {
+                  // dK and dV are out of TMEM: the next item may overwrite them.
+                  tc_fence_before();
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive(bar(L::bEpiDone));
+                }
+                auto f = [&](int e) { return sc * __uint_as_float(v[e]); };
+                // 32 BF16 values = 16-byte chunks 4 c .. 4 c + 3 of the 128-byte row.
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                  st_shared_v4(box + sw128_offset(lane, 4 * c + u), pack_bf16x2(f(8 * u), f(8 * u + 1)),
+                               pack_bf16x2(f(8 * u + 2), f(8 * u + 3)), pack_bf16x2(f(8 * u + 4), f(8 * u + 5)),
+                               pack_bf16x2(f(8 * u + 6), f(8 * u + 7)));
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int y = itm.k0 + 32 * static_cast<int>(quarter);
+            tma_store_3d_warp(&tmdK, dq_stage, 0, y, itm.bhk);
+            tma_store_3d_warp(&tmdV, dq_stage + 4096u, 0, y, itm.bhk);
+          }
+          ++kv;
         }
       }
     }
@@ -618,9 +672,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur = nxt;
       }
 
-      // ---------------- item epilogue: dK (x alpha), dV rows of this key tile ----------------
+      // ---------------- item epilogue (d = 128): dK (x alpha), dV rows of this key tile ----------------
       // The next item's dV(0) / dK(0), which overwrite these accumulators, wait for
       // its P^T(0) / dS^T(0), which this warp produces only after this epilogue.
+      // At d = 64 the drain warps store dK and dV instead.
+      if constexpr (!L::kTmaDQ) {
       if (ok) ok = wait_warp(bar(L::bMMADone), kv & 1, ctl);
       if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 25, kv);
       if (ok) {
@@ -651,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       }
+      }
     }
     asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
   }
@@ -667,8 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAUSAL>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                         cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                         const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D>;
   auto kern = attn_bwd_kernel<D, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
@@ -679,7 +736,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long n_items = static_cast<long long>((a.s.N + kTile - 1) / kTile) * a.s.B * a.s.Hkv;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, a);
+  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
   return cudaGetLastError();
 }
 
@@ -694,13 +751,13 @@ __global__ void convert_dq_kernel(const float4* __restrict__ src, uint2* __restr
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                       cudaStream_t stream) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
   if (a.s.d == 64)
-    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, a, stream)
-                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, a, stream);
-  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, a, stream)
-                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, a, stream);
+    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
+                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
+  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
+                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
 }
 
 // dQ = BF16(dQ workspace); n is a multiple of 4 (d is 64 or 128).

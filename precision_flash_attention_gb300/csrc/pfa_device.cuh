@@ -257,6 +257,19 @@ __device__ __forceinline__ void tma_reduce_add_3d_warp(const CUtensorMap* m, uin
       "r"(src), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// 3-D tiled store of a shared-memory box into global memory; elements outside
+// the tensor's extent are not written. The coordinates must be non-negative and
+// x x the element size a multiple of 16 bytes. Warp-collective; the elected lane
+// also commits the copy to its bulk group.
+__device__ __forceinline__ void tma_store_3d_warp(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];\n\t"
+      "@e cp.async.bulk.commit_group;\n\t}" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 // The elected lane waits until its committed bulk copies have finished reading
 // shared memory (read) or have completed (all); then the warp reconverges.
 __device__ __forceinline__ void bulk_wait_read_warp() {

@@ -58,10 +58,12 @@ cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long 
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const DeltaAltArgs& a, cudaStream_t stream);
 // tdq: FP32 [B*Hq, N, d] map of the dQ workspace with 32-column x 32-row boxes and
-// 128-byte swizzle (the reduce-add target of the d = 64 kernel).
+// 128-byte swizzle (the reduce-add target of the d = 64 kernel); tdk, tdv: BF16
+// [B*Hkv, N, d] maps of dK, dV with 64-column x 32-row boxes and 128-byte swizzle
+// (the store targets of the d = 64 kernel's drain warps).
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdArgs& a,
-                       cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                       const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream);
 
 }  // namespace pfa
