@@ -28,9 +28,9 @@ import torch  # noqa: E402
 METRIC = "attention fwd+bwd TFLOP/s and % of GB300 BF16 peak (GPT-2 shape, N=1k–8k)"
 WORKLOAD = dict(B=8, H=12, N=1024, d=64, causal=True, scale=0.125, beta=2.0, eps=1e-3)
 L2_FLUSH_BYTES = 256 << 20
-# Kernels of ours launched per step: attn_fwd, delta, attn_bwd, dQ convert (the
-# workspace zeroing is a memset on the stream, not a kernel of this library).
-LAUNCHES_PER_STEP = 4
+# Kernels of ours launched per step: attn_fwd, delta, the dQ workspace zeroing,
+# attn_bwd and the dQ conversion.
+LAUNCHES_PER_STEP = 5
 
 
 def flops(B, H, N, d, causal, which="fwd+bwd"):
@@ -271,8 +271,11 @@ class Step:
         self.bwd()
 
 
-def time_step(step, steps, warmup, flush):
-    """Per-phase CUDA-event timing on the launching stream; L2 flushed before each step."""
+def time_step(step, steps, warmup, flush, split=False):
+    """CUDA-event timing of whole steps on the launching stream; L2 flushed before each
+    step. The kernels of a step overlap their neighbours (programmatic dependent launch),
+    so events go only at the step's ends; with `split` they also go between the calls,
+    which serialises them, to give each call's own duration."""
     for _ in range(warmup):
         flush.fill_(1.0)
         step.run()
@@ -280,20 +283,24 @@ def time_step(step, steps, warmup, flush):
     rec = []
     for _ in range(steps):
         flush.fill_(1.0)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4 if split else 2)]
         e[0].record()
         step.fwd()
-        e[1].record()
+        if split:
+            e[1].record()
         step.delta_()
-        e[2].record()
+        if split:
+            e[2].record()
         step.bwd()
-        e[3].record()
+        e[-1].record()
         rec.append(e)
     torch.cuda.synchronize()
-    return {"fwd_ms": [a[0].elapsed_time(a[1]) for a in rec],
-            "delta_ms": [a[1].elapsed_time(a[2]) for a in rec],
-            "bwd_ms": [a[2].elapsed_time(a[3]) for a in rec],
-            "step_ms": [a[0].elapsed_time(a[3]) for a in rec]}
+    out = {"step_ms": [a[0].elapsed_time(a[-1]) for a in rec]}
+    if split:
+        out.update(fwd_ms=[a[0].elapsed_time(a[1]) for a in rec],
+                   delta_ms=[a[1].elapsed_time(a[2]) for a in rec],
+                   bwd_ms=[a[2].elapsed_time(a[3]) for a in rec])
+    return out
 
 
 def e2e_time(step, steps, warmup, flush):
@@ -392,7 +399,7 @@ def run_gpu_arm(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         # Interleave the modes so the cost of the fix is measured under the same conditions.
-        res = {m: {"fwd_ms": [], "delta_ms": [], "bwd_ms": [], "step_ms": []} for m in steps}
+        res = {m: {"step_ms": []} for m in steps}
         clk.mark_start()
         wall0 = time.perf_counter()
         for it in range(args.steps):
@@ -417,6 +424,10 @@ def run_gpu_arm(args):
                 if time.perf_counter() - tail0 > 4 * ClockSampler.PERIOD_MS * 1e-3:
                     break
             torch.cuda.synchronize()
+        # Each call's own duration: the same K steps again with events between the calls
+        # (not part of the step time above).
+        if not args.kernels_only:
+            split = {m: time_step(steps[m], args.steps, 0, flush, split=True) for m in steps}
     assert pfa.device_error() == 0, "device error word set during the benchmark"
     if args.kernels_only:
         # Profiling run: the kernels above are all it launches (no sweep, copies or CPU work).
@@ -435,7 +446,7 @@ def run_gpu_arm(args):
     value = world * f_total / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
 
-    fwd_ms, dl_ms, bwd_ms = (mean(res[head][k]) for k in ("fwd_ms", "delta_ms", "bwd_ms"))
+    fwd_ms, dl_ms, bwd_ms = (mean(split[head][k]) for k in ("fwd_ms", "delta_ms", "bwd_ms"))
     f_fwd, f_bwd = flops(B, H, N, d, True, "fwd"), flops(B, H, N, d, True, "bwd")
     dl_bytes = B * H * N * (4 * d + 4)
     kernels = {
@@ -466,8 +477,9 @@ def run_gpu_arm(args):
             for m in sorted({0, head}):
                 _progress(args, f"sweep N={n_s} mode {m}")
                 st = Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
-                r = time_step(st, max(3, args.steps // 2), 2, flush)
-                fm, bm, sm = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms", "step_ms"))
+                r = time_step(st, max(3, args.steps // 2), 2, flush, split=True)
+                fm, bm = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms"))
+                sm = statistics.median(time_step(st, max(3, args.steps // 2), 0, flush)["step_ms"])
                 tot = flops(B, H, n_s, d, True) / sm / 1e9
                 sweep[f"N={n_s},mode={m}"] = {
                     "fwd_tflops": flops(B, H, n_s, d, True, "fwd") / fm / 1e9,

@@ -241,7 +241,8 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   if ((rc = tile_map(&tdv, dv, B * H_kv, N, d, 32)) != PFA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
-  if ((rc = launched(cudaMemsetAsync(dq_accum, 0, ws, st))) != PFA_OK) return rc;
+  if ((rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
+    return rc;
   pfa::BwdArgs a;
   a.s = shape(B, H_q, H_kv, N, d, causal, scale);
   a.lse = lse;

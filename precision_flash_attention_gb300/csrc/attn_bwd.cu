@@ -192,6 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Setup done: let the next kernel on the stream be scheduled as CTAs leave, and
+  // order every global access after the kernel before this one.
+  grid_launch_dependents();
+  grid_dependency_wait();
   if (threadIdx.x == 32) PFA_BWD_TRACE(0, 30, 0);
   // Register split per warpgroup: launched with 80 per thread (768 x 80 =
   // 61440); warpgroup 0 and the drain warpgroup drop to 56 and the compute
@@ -736,11 +740,20 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long n_items = static_cast<long long>((a.s.N + kTile - 1) / kTile) * a.s.B * a.s.Hkv;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, tdq, tdk, tdv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, tdo, tdq, tdk, tdv, a);
+}
+
+__global__ void zero_kernel(float4* __restrict__ dst, long long n4) {
+  grid_launch_dependents();
+  grid_dependency_wait();   // the previous kernel may still read the buffer
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 __global__ void convert_dq_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, long long n4) {
+  grid_launch_dependents();
+  grid_dependency_wait();   // the workspace is the previous kernel's output
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const float4 x = src[i];
@@ -760,6 +773,17 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                     : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
 }
 
+// Zero the FP32 dQ workspace (n4 float4 values) as a kernel, so that it chains
+// with the kernels around it by programmatic dependent launch.
+cudaError_t launch_zero_workspace(float* ws, long long n4, cudaStream_t stream) {
+  const int threads = 256;
+  long long blocks = (n4 + threads - 1) / threads;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(zero_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    reinterpret_cast<float4*>(ws), n4);
+}
+
 // dQ = BF16(dQ workspace); n is a multiple of 4 (d is 64 or 128).
 cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream) {
   const long long n4 = n / 4;
@@ -767,9 +791,8 @@ cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cuda
   long long blocks = (n4 + threads - 1) / threads;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  convert_dq_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      reinterpret_cast<const float4*>(dq_accum), reinterpret_cast<uint2*>(dq), n4);
-  return cudaGetLastError();
+  return launch_pdl(convert_dq_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    reinterpret_cast<const float4*>(dq_accum), reinterpret_cast<uint2*>(dq), n4);
 }
 
 }  // namespace pfa

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
                                                     float* __restrict__ delta, long long rows) {
   constexpr int kRowsPerBlock = 256 / TPR;
   const int sub = threadIdx.x % TPR;
+  grid_launch_dependents();
+  grid_dependency_wait();   // O is the previous kernel's output
   // The loop condition depends only on the block's base row, so whole warps stay
   // together for the shuffles; rows past the end contribute nothing.
   for (long long base = blockIdx.x * static_cast<long long>(kRowsPerBlock); base < rows;
@@ -120,6 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Setup done: let the next kernel on the stream be scheduled as CTAs leave, and
+  // order every global access after the kernel before this one.
+  grid_launch_dependents();
+  grid_dependency_wait();
 
   if (*abort_flag == 0) {
     if (warp == 0) {
@@ -230,8 +236,7 @@ cudaError_t launch_alt_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const int n_t = (a.s.N + kTile - 1) / kTile;
   const dim3 grid(static_cast<unsigned>(n_t) * a.s.B * a.s.Hq);
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, tdo, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, tdo, a);
 }
 
 }  // namespace
@@ -244,13 +249,12 @@ cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long 
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   if (blocks > 152 * 8) blocks = 152 * 8;
   if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
   if (d == 64)
-    delta_kernel<8><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), delta, rows);
-  else
-    delta_kernel<16><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const uint4*>(o), static_cast<const uint4*>(dO), delta, rows);
-  return cudaGetLastError();
+    return launch_pdl(delta_kernel<8>, grid, dim3(threads), 0, stream, static_cast<const uint4*>(o),
+                      static_cast<const uint4*>(dO), delta, rows);
+  return launch_pdl(delta_kernel<16>, grid, dim3(threads), 0, stream, static_cast<const uint4*>(o),
+                    static_cast<const uint4*>(dO), delta, rows);
 }
 
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

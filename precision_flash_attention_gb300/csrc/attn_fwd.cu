@@ -159,6 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Setup done: let the next kernel on the stream be scheduled as CTAs leave, and
+  // order every global access after the kernel before this one.
+  grid_launch_dependents();
+  grid_dependency_wait();
   // Register split per warpgroup. The block is launched with 168 registers per
   // thread (384 x 168 = 64512). Warpgroup 0 (producers, MMA, one idle warp)
   // drops to 64 and the two softmax warpgroups rise to 216: 128 x 64 + 256 x 216
@@ -624,8 +628,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const int n_kt = (a.s.N + kTile - 1) / kTile;
   const long long n_items = static_cast<long long>((n_kt + 1) / 2) * a.s.B * a.s.Hq;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  kern<<<grid, kThreads, L::kBytes, stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, a);
 }
 
 template <int D, int MODE>

@@ -28,6 +28,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch. A kernel launched with launch_pdl() may start
+// while the kernel before it on the stream is still running; it runs its setup
+// (barriers, TMEM) and then calls grid_dependency_wait() before its first access
+// to global memory, which returns once that kernel has completed and its writes
+// are visible (immediately when there is none). grid_launch_dependents() lets
+// the next kernel on the stream be scheduled onto SMs as this one's CTAs leave.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -9,6 +9,25 @@
 
 namespace pfa {
 
+// Launches `kern` on `stream` as a programmatic dependent of the kernel before
+// it: the two may overlap, and `kern` orders its global memory accesses after
+// the previous kernel with grid_dependency_wait() (pfa_device.cuh).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 
 // Arguments common to the tiled kernels (all sizes in elements).
@@ -65,5 +84,8 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream);
+// Zeroes n4 float4 values of the dQ workspace on `stream` (a kernel, so that it
+// overlaps its neighbours by programmatic dependent launch).
+cudaError_t launch_zero_workspace(float* ws, long long n4, cudaStream_t stream);
 
 }  // namespace pfa
