@@ -546,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------- epilogue ----------------
       if (ok) ok = wait_warp(bar(L::bODone + t), ot & 1, ctl);
+      if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 9, ot);
       if (ok) {
         tc_fence_after();
         // The flag is exact after every tile, so the shift in use is the final one.
@@ -574,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[qd] = make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
           }
         }
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 10, ot);
         if (row_ok) args.lse[static_cast<size_t>(bh) * N + qrow] = m_fin + lg2_approx(l) * kLn2;
         if (COUNT) {
           // BF16(Pbar) == 1 under the final shift: entries within tau of m1,
