@@ -31,6 +31,12 @@
  *  - Kernels never trap. A kernel whose internal pipeline wait exceeds about one
  *    second gives up, sets a bit in the library's device error word and returns;
  *    pfa_device_error() reads that word.
+ *  - Every kernel is launched as a programmatic dependent of the work before it
+ *    on `stream`: it may start its setup while the previous kernel finishes, but
+ *    touches no global memory until that kernel has completed, so stream order
+ *    is kept. It also lets the next kernel on the stream start early; a caller's
+ *    kernel launched the same way must wait (griddepcontrol.wait) before reading
+ *    this library's outputs.
  */
 #ifndef PFA_H_
 #define PFA_H_
