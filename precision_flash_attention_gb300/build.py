@@ -10,6 +10,7 @@ from __future__ import annotations
 import hashlib
 import os
 import platform
+import re
 import shutil
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
@@ -54,8 +55,9 @@ KERNEL_SOURCES = {"attn_bwd_kernel": "attn_bwd.cu", "convert_dq_kernel": "attn_b
 
 
 def _product_text(path: str) -> bytes:
-    """A source file without what only trace builds (-DPFA_TRACE) compile: lines that
-    invoke a trace macro and `#if defined(PFA_TRACE) ...` blocks."""
+    """A source file as the product build compiles it: without comments and without
+    what only trace builds (-DPFA_TRACE) compile (lines that invoke a trace macro and
+    `#if defined(PFA_TRACE) ...` blocks)."""
     out, depth = [], 0
     with open(path, encoding="utf-8") as f:
         for line in f:
@@ -72,7 +74,9 @@ def _product_text(path: str) -> bytes:
             if "_TRACE(" in t and "define" not in t:
                 continue
             out.append(line)
-    return "".join(out).encode()
+    text = re.sub(r"/\*.*?\*/", "", "".join(out), flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return text.encode()
 
 
 def kernel_source_digest(kernel: str) -> str:
