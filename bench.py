@@ -506,10 +506,7 @@ def run_gpu_arm(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.25) Q/K/V, N(0,1e-4) dO)",
-        "config": {"workload": "GPT-2-small attention layer fwd+bwd", "B": B, "H": H, "N": N,
-                   "d": d, "causal": True, "fix_mode": head, "beta": w["beta"], "eps": w["eps"],
-                   "l2": "flushed (256 MiB write) before every step",
-                   "parallelism": f"replicas x{world}"},
+        "config": dict(workload_config(world, head), l2="flushed (256 MiB write) before every step"),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(steps),
         "clocks": clk.summary(), "wall_s_timed_region": wall,
@@ -519,6 +516,13 @@ def run_gpu_arm(args):
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def workload_config(world, mode):
+    """The `config` object both arms report for the bench workload."""
+    return {"workload": "GPT-2-small attention layer fwd+bwd", "B": WORKLOAD["B"], "H": WORKLOAD["H"],
+            "N": WORKLOAD["N"], "d": WORKLOAD["d"], "causal": WORKLOAD["causal"], "fix_mode": mode,
+            "beta": WORKLOAD["beta"], "eps": WORKLOAD["eps"], "parallelism": f"replicas x{world}"}
 
 
 def run_reference_arm(args):
@@ -538,9 +542,7 @@ def run_reference_arm(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": "GPT-2-small attention layer fwd+bwd",
-                                        "B": 8, "H": 12, "N": 1024, "d": 64, "causal": True,
-                                        "fix_mode": args.mode},
+        "data": "synthetic", "config": workload_config(world, args.mode),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                          "sample": "4 of 96 (b,h) heads per step, fwd+delta+bwd, float64 numpy"},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
