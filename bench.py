@@ -506,7 +506,7 @@ def run_gpu_arm(args):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.25) Q/K/V, N(0,1e-4) dO)",
-        "config": dict(workload_config(world, head), l2="flushed (256 MiB write) before every step"),
+        "config": dict(workload_config(world, head, w), l2="flushed (256 MiB write) before every step"),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(steps),
         "clocks": clk.summary(), "wall_s_timed_region": wall,
@@ -518,11 +518,11 @@ def run_gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
-def workload_config(world, mode):
-    """The `config` object both arms report for the bench workload."""
-    return {"workload": "GPT-2-small attention layer fwd+bwd", "B": WORKLOAD["B"], "H": WORKLOAD["H"],
-            "N": WORKLOAD["N"], "d": WORKLOAD["d"], "causal": WORKLOAD["causal"], "fix_mode": mode,
-            "beta": WORKLOAD["beta"], "eps": WORKLOAD["eps"], "parallelism": f"replicas x{world}"}
+def workload_config(world, mode, w=WORKLOAD):
+    """The `config` object both arms report for the bench workload `w`."""
+    return {"workload": "GPT-2-small attention layer fwd+bwd", "B": w["B"], "H": w["H"], "N": w["N"],
+            "d": w["d"], "causal": w["causal"], "fix_mode": mode, "beta": w["beta"], "eps": w["eps"],
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference_arm(args):
