@@ -128,6 +128,18 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
                  float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
                  pfa_stream_t stream);
 
+/* The backward kernel alone, accumulating dQ in FP32 (no counterpart in the
+ * paper): dq_accum += alpha dS K, and dK, dV (BF16) are written, with the same
+ * arguments, equations and checks as pfa_attn_bwd. dq_accum is [B, H_q, N, d]
+ * FP32, caller-owned device memory, 16-byte aligned; it is neither zeroed nor
+ * converted. For gradient accumulation across calls (micro-batches or chunks of
+ * keys), or to keep dQ in FP32. pfa_attn_bwd is: zero the workspace, this
+ * call, convert the workspace to BF16. */
+int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                       const float* lse, const float* delta, float* dq_accum, pfa_bf16* dk,
+                       pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                       pfa_stream_t stream);
+
 /* The same backward pass for callers that cannot allocate device memory (no
  * counterpart in the paper; this is a deployment convenience). Some callers are
  * not allowed to call cudaMalloc at all: runtimes that reserve all device memory

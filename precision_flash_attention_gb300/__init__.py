@@ -15,12 +15,13 @@ import math
 
 import torch
 
-from ._lib import (EXPORTS, PfaError, attn_bwd, attn_bwd_noalloc, attn_delta, attn_delta_alt,
+from ._lib import (EXPORTS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_noalloc, attn_delta, attn_delta_alt,
                    attn_fwd, bwd_workspace_bytes, device_error, device_error_site, load,
                    status_string)
 
 __all__ = [
-    "EXPORTS", "PfaError", "attn_fwd", "attn_delta", "attn_delta_alt", "attn_bwd", "attn_bwd_noalloc",
+    "EXPORTS", "PfaError", "attn_fwd", "attn_delta", "attn_delta_alt", "attn_bwd", "attn_bwd_accum",
+    "attn_bwd_noalloc",
     "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "forward", "backward",
     "StabilizedAttention", "new_counters",
 ]

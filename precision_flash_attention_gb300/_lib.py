@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED"
 
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
-           "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
+           "pfa_attn_bwd_accum", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
            "pfa_last_error", "pfa_device_error", "pfa_device_error_site")
 
 
@@ -59,6 +59,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.pfa_attn_bwd.restype = i
     lib.pfa_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.pfa_attn_bwd_accum.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    lib.pfa_attn_bwd_accum.restype = i
     lib.pfa_attn_bwd_noalloc.restype = i
     lib.pfa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.pfa_bwd_workspace_bytes.restype = sz
@@ -161,6 +163,23 @@ def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, sca
                              _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, k.shape[1], N, d,
                              int(bool(causal)), float(scale), _stream(stream))
     _check(st, "pfa_attn_bwd")
+
+
+def attn_bwd_accum(q, k, v, do, lse, delta, dq_accum, dk, dv, *, causal: bool, scale: float,
+                   stream=None) -> None:
+    """pfa_attn_bwd_accum: dq_accum (FP32 [B, H_q, N, d]) += alpha dS K; dk, dv written."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do"), (dk, "dk"), (dv, "dv")):
+        _bhnd(t, n)
+    _bhnd(lse, "lse", torch.float32, 3)
+    _bhnd(delta, "delta", torch.float32, 3)
+    _bhnd(dq_accum, "dq_accum", torch.float32)
+    B, Hq, N, d = q.shape
+    if dq_accum.shape != q.shape:
+        raise ValueError("dq_accum must have the shape of q")
+    st = load().pfa_attn_bwd_accum(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
+                                   _ptr(dq_accum), _ptr(dk), _ptr(dv), B, Hq, k.shape[1], N, d,
+                                   int(bool(causal)), float(scale), _stream(stream))
+    _check(st, "pfa_attn_bwd_accum")
 
 
 def attn_bwd_noalloc(q, k, v, do, lse, delta, dq, dk, dv, *, causal: bool, scale: float,

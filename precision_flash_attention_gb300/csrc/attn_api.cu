@@ -214,36 +214,48 @@ size_t pfa_bwd_workspace_bytes(int B, int H_q, int N, int d) {
   return static_cast<size_t>(B) * H_q * N * d * sizeof(float);
 }
 
-int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
-                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
-                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
-                 pfa_stream_t stream) {
-  if (!q || !k || !v || !dO || !lse || !delta || !dq || !dk || !dv || !dq_accum)
-    return PFA_ERR_INVALID_ARG;
-  int rc = check_sizes(B, H_q, H_kv, N, d);
+}  // extern "C"
+
+namespace {
+
+// Everything the backward kernel's launch needs, checked and encoded before any
+// launch, so that an argument error leaves the stream untouched.
+struct BwdLaunch {
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
+  pfa::BwdArgs a;
+};
+
+// The argument checks shared by pfa_attn_bwd and pfa_attn_bwd_accum, and the
+// tensor maps and arguments of the kernel (dq_accum += alpha dS K; dk, dv written).
+int bwd_check(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+              const float* lse, const float* delta, const float* dq_accum, const pfa_bf16* dk,
+              const pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d, float scale) {
+  if (!q || !k || !v || !dO || !lse || !delta || !dk || !dv || !dq_accum) return PFA_ERR_INVALID_ARG;
+  const int rc = check_sizes(B, H_q, H_kv, N, d);
   if (rc != PFA_OK) return rc;
   if (!good_scale(scale)) return PFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
-      !aligned16(delta) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      !aligned16(dq_accum))
+      !aligned16(delta) || !aligned16(dk) || !aligned16(dv) || !aligned16(dq_accum))
     return PFA_ERR_MISALIGNED;
+  return PFA_OK;
+}
+
+int bwd_prepare(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                const float* lse, const float* delta, float* dq_accum, pfa_bf16* dk, pfa_bf16* dv,
+                int B, int H_q, int H_kv, int N, int d, int causal, float scale, BwdLaunch* L) {
+  int rc = bwd_check(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, scale);
+  if (rc != PFA_OK) return rc;
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != PFA_OK) return rc;
-  CUtensorMap tq, tk, tv, tdo;
-  if ((rc = tile_map(&tq, q, B * H_q, N, d)) != PFA_OK) return rc;
-  if ((rc = tile_map(&tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
-  if ((rc = tile_map(&tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
-  if ((rc = tile_map(&tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
-  CUtensorMap tdq, tdk, tdv;
-  if ((rc = f32_box_map(&tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&L->tq, q, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&L->tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&L->tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
+  if ((rc = tile_map(&L->tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
+  if ((rc = f32_box_map(&L->tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
   // dK, dV leave through 64-column x 32-row boxes (d = 64: one drain warp's rows).
-  if ((rc = tile_map(&tdk, dk, B * H_kv, N, d, 32)) != PFA_OK) return rc;
-  if ((rc = tile_map(&tdv, dv, B * H_kv, N, d, 32)) != PFA_OK) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
-  if ((rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
-    return rc;
-  pfa::BwdArgs a;
+  if ((rc = tile_map(&L->tdk, dk, B * H_kv, N, d, 32)) != PFA_OK) return rc;
+  if ((rc = tile_map(&L->tdv, dv, B * H_kv, N, d, 32)) != PFA_OK) return rc;
+  pfa::BwdArgs& a = L->a;
   a.s = shape(B, H_q, H_kv, N, d, causal, scale);
   a.lse = lse;
   a.delta = delta;
@@ -252,8 +264,46 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   a.dv = dv;
   a.err = dev->err;
   a.err_site = dev->site;
-  if ((rc = launched(pfa::launch_bwd(tq, tk, tv, tdo, tdq, tdk, tdv, a, st))) != PFA_OK) return rc;
+  return PFA_OK;
+}
+
+int bwd_launch(const BwdLaunch& L, cudaStream_t st) {
+  return launched(pfa::launch_bwd(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdk, L.tdv, L.a, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                 pfa_stream_t stream) {
+  if (!dq) return PFA_ERR_INVALID_ARG;
+  int rc = bwd_check(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, scale);
+  if (rc != PFA_OK) return rc;
+  if (!aligned16(dq)) return PFA_ERR_MISALIGNED;
+  BwdLaunch L;
+  if ((rc = bwd_prepare(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, causal, scale,
+                        &L)) != PFA_OK)
+    return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
+  if ((rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
+    return rc;
+  if ((rc = bwd_launch(L, st)) != PFA_OK) return rc;
   return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
+}
+
+int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                       const float* lse, const float* delta, float* dq_accum, pfa_bf16* dk, pfa_bf16* dv,
+                       int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                       pfa_stream_t stream) {
+  BwdLaunch L;
+  const int rc =
+      bwd_prepare(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, causal, scale, &L);
+  if (rc != PFA_OK) return rc;
+  return bwd_launch(L, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* pfa_status_string(int status) {

@@ -302,3 +302,35 @@ def test_stream_and_autograd_wrapper():
     ref = oracle_full({n: x.cpu() for n, x in t.items()}, causal=True, scale=0.125, fix_mode=1)
     assert_fwd_close({"o": f64(o), "lse": ref["lse"]}, ref)
     assert_bwd_close({"dq": f64(q.grad), "dk": f64(k.grad), "dv": f64(v.grad)}, ref)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 2, 300, 64), (1, 2, 1, 200, 128)], ids=["d64-gqa", "d128"])
+def test_bwd_accumulate_entry_point(shape):
+    # pfa_attn_bwd_accum adds alpha dS K into a caller's FP32 buffer and writes dK, dV;
+    # two calls on one buffer give twice dQ, and dK, dV match pfa_attn_bwd.
+    B, Hq, Hkv, N, d = shape
+    t = to_dev(inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.5, std_do=1.0, seed=7))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = pfa.forward(t["q"], t["k"], t["v"], causal=True, scale=scale)
+    dq, dk, dv, delta = pfa.backward(t["q"], t["k"], t["v"], o, lse, t["do"], causal=True, scale=scale)
+    acc = torch.zeros(t["q"].shape, dtype=torch.float32, device="cuda")
+    dk2, dv2 = torch.empty_like(dk), torch.empty_like(dv)
+    for _ in range(2):
+        pfa.attn_bwd_accum(t["q"], t["k"], t["v"], t["do"], lse, delta, acc, dk2, dv2, causal=True,
+                           scale=scale)
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    assert torch.equal(dk2, dk) and torch.equal(dv2, dv)
+    half = acc / 2
+    assert torch.isfinite(half).all()
+    # The BF16 dQ of pfa_attn_bwd is the rounded FP32 accumulation of one call.
+    assert rel_l2(f64(half.to(torch.bfloat16)), f64(dq)) < 1e-2
+    ref = oracle_full({n: x.cpu() for n, x in t.items()}, causal=True, scale=scale, fix_mode=0)
+    assert rel_l2(f64(half), ref["dq"]) <= TOL_BWD_REL
+    # An argument error launches nothing and returns the code.
+    lib = pfa.load()
+    import ctypes
+    st = lib.pfa_attn_bwd_accum(*([ctypes.c_void_p(t["q"].data_ptr())] * 6), None,
+                                ctypes.c_void_p(dk2.data_ptr()), ctypes.c_void_p(dv2.data_ptr()),
+                                B, Hq, Hkv, N, d, 1, scale, None)
+    assert st == -1 and "INVALID_ARG" in pfa.status_string(st)
