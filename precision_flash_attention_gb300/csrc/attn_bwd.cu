@@ -11,26 +11,28 @@
 // pass (priors.kr, the fix paragraph; bud-325 note, Results): P is recomputed
 // from the saved lse whatever shift the forward pass used.
 //
-// Persistent: one CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...
-// in heavy-first order (key tile 0 has the most causal work). Barrier phases
+// Persistent: one CTA per SM takes items in heavy-first order (key tile 0 has
+// the most causal work), dealt in serpentine rounds of gridDim.x. Barrier phases
 // count the CTA's query tiles across items, so an item's first products start
 // while the previous item's last dQ is drained and its dK / dV are stored, and
 // setup and teardown happen once per SM.
 //
 // 768 threads in six warpgroups: warp 0 Q / dO producer (TMA), warp 1 TMEM
 // owner and tcgen05.mma issuer, warp 2 K / V producer, warp 3 idle; warps 4-19
-// compute (P^T, dS^T); warps 20-23 drain dQ out of TMEM. Compute warp w owns TMEM lane quarter w % 4
+// compute (P^T, dS^T); warps 20-23 drain dQ out of TMEM and, at d = 64, store
+// each item's dK and dV through TMA. Compute warp w owns TMEM lane quarter w % 4
 // (32 keys) and query group (w - 4) / 4 (32 queries), so each SM sub-partition
-// runs four compute warps whose latencies overlap; drain warp w owns query rows
-// of lane quarter w % 4 and all d columns of dQ.
+// runs four compute warps whose latencies overlap; drain warp w owns the rows of
+// lane quarter w % 4 and all d columns of dQ (and of dK, dV).
 // P^T and dS^T are cast to BF16 and written back into TMEM over S^T and dP^T
 // (each query group over its own input columns), where they are the A operands
 // of dV and dK; dS^T also goes to a 128B-swizzled shared buffer that the dQ
 // product reads as its (M = queries) A operand.
 // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,256+d), dK [256+d,256+2d),
 // dQ [384,448) for d = 64 and over dP^T [128,256) for d = 128.
-// Tensor-core order per query tile i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1),
-// so the next tile's scores are ready when the compute warps finish dS(i).
+// Tensor-core order per query tile i: dV(i), S^T(i+1), dK(i), then at d = 64
+// dP^T(i+1) and dQ(i), at d = 128 (dQ over dP^T) dQ(i) and dP^T(i+1), so the next
+// tile's scores are ready when the compute warps finish dS(i).
 #include "pfa_device.cuh"
 #include "pfa_trace.cuh"
 

@@ -10,9 +10,9 @@
 // equations, and the fix of paper §4) and the bud-325 note of the same title
 // (Key claims, Method / Algorithm 1).
 //
-// A work item is two 128-row Q tiles (t = 0, 1) of one (batch, query head).
-// Persistent: one CTA per SM takes items blockIdx.x, blockIdx.x + gridDim.x, ...
-// heaviest causal pairs first; barrier phases count across items, so setup and
+// A work item is two adjacent 128-row Q tiles (t = 0, 1) of one (batch, query
+// head). Persistent: one CTA per SM takes items heaviest causal pairs first,
+// dealt in serpentine rounds of gridDim.x; barrier phases count across items, so setup and
 // teardown happen once per SM and the next item's Q (double buffered for
 // d = 64) and K / V stream in while the current item finishes. 384 threads,
 // one warpgroup per role group (registers are granted per warpgroup):
