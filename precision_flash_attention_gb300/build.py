@@ -76,7 +76,8 @@ def _product_text(path: str) -> bytes:
             out.append(line)
     text = re.sub(r"/\*.*?\*/", "", "".join(out), flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return text.encode()
+    # Layout does not change what is compiled: one stripped, non-empty line per line.
+    return "\n".join(t.strip() for t in text.splitlines() if t.strip()).encode()
 
 
 def kernel_source_digest(kernel: str) -> str:
