@@ -296,11 +296,6 @@ __device__ __forceinline__ void bulk_wait_all_warp() {
   __syncwarp();
 }
 
-// Named barrier over `count` threads (a multiple of 32); id 0 is __syncthreads.
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // Prefetch a 3-D tile into L2 (no shared memory, no completion to wait for);
 // warp-collective like the loads.
 __device__ __forceinline__ void tma_prefetch_l2_3d_warp(const CUtensorMap* m, int x, int y, int z) {
