@@ -445,95 +445,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Two entries of the tile reach a threshold iff two of the eight 16-column
         // blocks do or two of the sixteen column classes (column mod 16) do: a
         // single qualifying entry lies in one block and one class, and two
-        // distinct entries differ in their block or in their class. So the block
-        // maxima and the class maxima settle it without a data-dependent scan.
+        // distinct entries differ in their block or in their class. The block
+        // count is known with the maximum; the class maxima are gathered during
+        // the exponentials. A new maximum alone in its block is taken as single
+        // until they show otherwise, and a row found repeated then has its tile
+        // recomputed under the repeated shift (a second pass, taken only when a
+        // tie sits inside one block of a new maximum).
         bool jump = false;
+        int nb = 0;
+        float thr_eps = 0.f;
+        bool rep_use = rep;
         if (kTies) {
-          const float thr_eps = t1 - args.eps_raw;
+          thr_eps = t1 - args.eps_raw;
           jump = t1 > m1 && m1 < thr_eps;
-          bool two = false;
-          if (__any_sync(0xFFFFFFFFu, jump)) {
-            int nb = 0, ne = 0;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              auto x = [&](int k) { return __uint_as_float(v[16 * k + e]); };
-              const float ce = fmaxf(fmax3(x(0), x(1), x(2)), fmax3(x(3), fmax3(x(4), x(5), x(6)), x(7)));
-              ne += ce >= thr_eps ? 1 : 0;
-            }
-            two = nb >= 2 || ne >= 2;
-          }
+          for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
           if (t1 > m1) {
-            rep = jump ? two : true;
+            rep_use = jump ? nb >= 2 : true;
           } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
-            rep = true;
+            rep_use = true;
           }
         }
         const float m1_old = m1;
         m1 = fmaxf(m1, t1);
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 5, j);
 
-        const float m_new = shift_of(m1, rep);
-        const bool changed = (j > 0) && (m_new != m_sh);
-        if constexpr (L::kSplitP) {
-          // Obar_t and the Pbar_t columns are free once the previous key tile's
-          // product has completed (tile 0 of an item: its epilogue waited for
-          // the last product of the previous item).
-          // A failed wait ends the loop at the bottom of this iteration: a break
-          // here, with all the scores live, defeats register allocation.
-          if (j > 0) {
-            ok = wait_warp(bar(L::bPVDone + t), (ct + j - 1) & 1, ctl);
-            tc_fence_after();
+        // Pbar = exp(S - m) in FP32; l sums it; the BF16 casts go to TMEM.
+        const float l0s = l0, l1s = l1;
+        float m_new = m_sh, corr = 1.f;
+        bool changed = false;
+        int cnt_tile = 0;
+#pragma unroll 1
+        for (int pass = 0;; ++pass) {
+          m_new = shift_of(m1, rep_use);
+          changed = (j > 0) && (m_new != m_sh);
+          corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
+          l0 = l0s * corr;
+          l1 = l1s * corr;
+          const float nml2 = -m_new * kLog2e;
+          const float thr = m1 - args.tau_raw;
+          cnt_tile = 0;
+          float ce[16];   // class maxima (column mod 16)
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+              const float x0 = __uint_as_float(v[64 * half + 2 * u]);
+              const float x1 = __uint_as_float(v[64 * half + 2 * u + 1]);
+              if (COUNT) cnt_tile += (x0 >= thr) + (x1 >= thr);
+              float y0, y1;
+              fma2(y0, y1, x0, x1, sl2, nml2);
+              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+              add2(l0, l1, p0, p1);
+              pk[u] = pack_bf16x2(p0, p1);
+            }
+            if (kTies) {
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                auto x = [&](int k) { return __uint_as_float(v[64 * half + 16 * k + e]); };
+                const float c4 = fmaxf(fmax3(x(0), x(1), x(2)), x(3));
+                ce[e] = half ? fmaxf(ce[e], c4) : c4;
+              }
+            }
+            if constexpr (L::kSplitP) {
+              // Obar_t and the Pbar_t columns are free once the previous key
+              // tile's product has completed (tile 0 of an item: its epilogue
+              // waited for the last product of the previous item). Without split
+              // Pbar, S_t of this tile was committed after that product.
+              // A failed wait ends the loop at the bottom of this iteration.
+              if (half == 0 && pass == 0 && j > 0) {
+                ok = wait_warp(bar(L::bPVDone + t), (ct + j - 1) & 1, ctl);
+                tc_fence_after();
+              }
+            }
+            tmem_st32(tP + 32 * half, pk);
           }
+          if (!kTies || pass > 0) break;
+          const bool single = jump && nb < 2;
+          if (!__any_sync(0xFFFFFFFFu, single)) break;
+          int ne = 0;
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ne += ce[e] >= thr_eps ? 1 : 0;
+          const bool wrong = single && ne >= 2;
+          if (wrong) rep_use = true;
+          // Mode 0 keeps the flag for the counter only: its shift does not move.
+          if (MODE == 0 || !__any_sync(0xFFFFFFFFu, wrong)) break;
+          tmem_st_wait();   // the second pass stores over the first one's Pbar
         }
-        const float corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
-        l0 *= corr;
-        l1 *= corr;
+        rep = rep_use;
         m_sh = m_new;
-
-        // Rescale Obar where the shift moved. The previous P.V of this tile has
-        // completed: split Pbar waited for it above, otherwise S_t of this tile
-        // was committed after it.
+        if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
+        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 6, j);
+        // Rescale Obar where the shift moved: the scores are dead, so one TMEM
+        // round trip covers 64 columns.
         if (__any_sync(0xFFFFFFFFu, changed)) {
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(tO + c, o);
-            tmem_ld_wait32(o);
+          for (int c = 0; c < D; c += 64) {
+            uint32_t o[64];
+            tmem_ld64(tO + c, o);
+            tmem_ld_wait64(o);
 #pragma unroll
-            for (int u = 0; u < 32; u += 2) {
+            for (int u = 0; u < 64; u += 2) {
               float y0 = __uint_as_float(o[u]), y1 = __uint_as_float(o[u + 1]);
               mul2(y0, y1, corr);
               o[u] = __float_as_uint(y0);
               o[u + 1] = __float_as_uint(y1);
             }
-            tmem_st32(tO + c, o);
+            tmem_st64(tO + c, o);
           }
         }
-
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 6, j);
-        // Pbar = exp(S - m) in FP32; l sums it; the BF16 cast goes to TMEM over S.
-        const float nml2 = -m_sh * kLog2e;
-        const float thr = m1 - args.tau_raw;
-        int cnt_tile = 0;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float x0 = __uint_as_float(v[64 * half + 2 * u]);
-            const float x1 = __uint_as_float(v[64 * half + 2 * u + 1]);
-            if (COUNT) cnt_tile += (x0 >= thr) + (x1 >= thr);
-            float y0, y1;
-            fma2(y0, y1, x0, x1, sl2, nml2);
-            const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-            add2(l0, l1, p0, p1);
-            pk[u] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(tP + 32 * half, pk);
-        }
-        if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
         tmem_st_wait();
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 7, j);
         tc_fence_before();

@@ -454,6 +454,19 @@ __device__ __forceinline__ void tmem_ld_wait64(uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : PFA_W64 : : "memory");
 }
 
+#define PFA_S64 PFA_S8(0), PFA_S8(8), PFA_S8(16), PFA_S8(24), PFA_S8(32), PFA_S8(40), PFA_S8(48), PFA_S8(56)
+// r[0..63] into 32 lanes x 64 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,"
+      "%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,"
+      "%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};" ::"r"(taddr),
+      PFA_S64
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
