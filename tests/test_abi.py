@@ -50,6 +50,13 @@ def test_workspace_bytes(lib):
 A = 1 << 20  # a fake, 16-byte aligned "device" address; never dereferenced on these paths
 
 
+def _no_device():
+    """Calls that pass validation would launch kernels on the fake addresses: they are
+    made only where no CUDA device exists, so they fail on the device lookup."""
+    import torch
+    return not torch.cuda.is_available()
+
+
 def _fwd(lib, **kw):
     args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=1, N=64, d=64, causal=0, scale=0.125,
                 mode=1, beta=2.0, eps=1e-3, counters=None, stream=None)
@@ -74,10 +81,11 @@ def test_fwd_argument_errors(lib):
     assert _fwd(lib, scale=float("nan")) == inv
     assert _fwd(lib, q=A + 8) == mis
     assert _fwd(lib, counters=A + 4) == mis
+    assert _fwd(lib, mode=0, eps=-1.0, counters=A) == inv
     # beta is not checked in mode 0/2, eps not in mode 0 without counters: the call gets
     # past validation and fails only on the missing device.
-    assert _fwd(lib, mode=0, beta=0.5, eps=-1.0) not in (inv, mis)
-    assert _fwd(lib, mode=0, eps=-1.0, counters=A) == inv
+    if _no_device():
+        assert _fwd(lib, mode=0, beta=0.5, eps=-1.0) not in (inv, mis)
 
 
 def test_other_entry_points_validate(lib):
@@ -100,8 +108,40 @@ def test_other_entry_points_validate(lib):
 
 
 def test_without_a_device_calls_fail_cleanly(lib):
-    import torch
-    if torch.cuda.is_available():
+    if not _no_device():
         pytest.skip("a device is present")
     assert _fwd(lib) in (-3, -4)
     assert lib.pfa_device_error(0) in (-3, -4)
+
+
+def test_accumulate_and_noalloc_entry_points_validate(lib):
+    inv, mis, too_large = -1, -2, -6
+    # pfa_attn_bwd_accum: the same checks as pfa_attn_bwd, before any device call.
+    args = [A] * 9 + [1, 2, 1, 64, 64, 1, 0.125, None]
+    for i in range(9):
+        bad = list(args)
+        bad[i] = None
+        assert lib.pfa_attn_bwd_accum(*bad) == inv, i
+    bad = list(args)
+    bad[6] = A + 4                       # the FP32 accumulator, misaligned
+    assert lib.pfa_attn_bwd_accum(*bad) == mis
+    bad = list(args)
+    bad[11] = 3                          # H_kv does not divide H_q
+    assert lib.pfa_attn_bwd_accum(*bad) == inv
+    bad = list(args)
+    bad[13] = 32                         # d not in {64, 128}
+    assert lib.pfa_attn_bwd_accum(*bad) == inv
+    bad = list(args)
+    bad[15] = float("inf")               # scale
+    assert lib.pfa_attn_bwd_accum(*bad) == inv
+    # pfa_attn_bwd_noalloc: sizes are checked first, then the fixed buffer's limit.
+    nargs = [A] * 9 + [1, 2, 1, 64, 64, 1, 0.125, None]
+    bad = list(nargs)
+    bad[13] = 96
+    assert lib.pfa_attn_bwd_noalloc(*bad) == inv
+    bad = list(nargs)
+    bad[9], bad[10], bad[11], bad[12] = 8, 16, 8, 8192   # 8*16*8192*64 values > 8,388,608
+    assert lib.pfa_attn_bwd_noalloc(*bad) == too_large
+    if _no_device():
+        bad[12] = 1024                                   # 8*16*1024*64 = 8,388,608: fits
+        assert lib.pfa_attn_bwd_noalloc(*bad) != too_large
