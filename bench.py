@@ -486,10 +486,7 @@ def run_gpu_arm(args):
 
     mean = lambda xs: sum(xs) / len(xs)  # noqa: E731
     ms = mean(res[head]["step_ms"])
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     B, H, N, d = w["B"], w["H"], w["N"], w["d"]
     f_total = flops(B, H, N, d, True)
     value = world * f_total / (ms * 1e-3) / 1e12
@@ -572,6 +569,16 @@ def run_gpu_arm(args):
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the slowest rank's step time sets the job's
+    time); `x` itself on one rank. Every rank must call it."""
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
 
 
 def workload_config(world, mode, w=WORKLOAD):
