@@ -179,11 +179,22 @@ int pfa_device_error(int clear);
 
 /* Where the first bounded wait that gave up (PFA_DEVERR_TIMEOUT) since the last
  * pfa_device_error(1) was: 0 if none, else kernel id in bits 56-59 (1 forward,
- * 2 backward, 3 delta via dP o P), bit 55 set for a teardown (drain) wait,
+ * 2 backward, 3 delta via dP o P, 4 pfa_wait_probe), bit 55 set for a teardown
+ * (drain) wait,
  * bit 54 the awaited phase parity, bits 32-53 the barrier's byte offset in the
  * kernel's shared memory, bits 0-31 blockIdx.x. Negative: a PFA_ERR_* code.
  * Synchronises the current device. */
 long long pfa_device_error_site(void);
+
+/* Self-test of the failure path (no counterpart in the paper). Enqueues on
+ * `stream` one warp that waits on a shared-memory mbarrier nothing completes; the
+ * wait is bounded like every pipeline wait of the library, so after about a
+ * second the warp gives up, records its site (kernel id 4, offset 0, parity 0)
+ * and sets PFA_DEVERR_TIMEOUT in the device error word. No fault or trap is
+ * raised and the device stays usable. Read the result with pfa_device_error and
+ * pfa_device_error_site, and clear it with pfa_device_error(1). Returns PFA_OK,
+ * PFA_ERR_UNSUPPORTED or PFA_ERR_LAUNCH. */
+int pfa_wait_probe(pfa_stream_t stream);
 
 #ifdef __cplusplus
 }

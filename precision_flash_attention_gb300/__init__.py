@@ -17,12 +17,13 @@ import torch
 
 from ._lib import (EXPORTS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_noalloc, attn_delta, attn_delta_alt,
                    attn_fwd, bwd_workspace_bytes, device_error, device_error_site, load,
-                   status_string)
+                   status_string, wait_probe)
 
 __all__ = [
     "EXPORTS", "PfaError", "attn_fwd", "attn_delta", "attn_delta_alt", "attn_bwd", "attn_bwd_accum",
     "attn_bwd_noalloc",
-    "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "forward", "backward",
+    "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "wait_probe",
+    "forward", "backward",
     "StabilizedAttention", "new_counters",
 ]
 

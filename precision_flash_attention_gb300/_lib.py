@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED"
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
            "pfa_attn_bwd_accum", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
-           "pfa_last_error", "pfa_device_error", "pfa_device_error_site")
+           "pfa_last_error", "pfa_device_error", "pfa_device_error_site", "pfa_wait_probe")
 
 
 class PfaError(RuntimeError):
@@ -72,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_device_error_site.restype = ctypes.c_longlong
     lib.pfa_device_error.argtypes = [i]
     lib.pfa_device_error.restype = i
+    lib.pfa_wait_probe.argtypes = [vp]
+    lib.pfa_wait_probe.restype = i
     if path is None:
         _LIB = lib
     return lib
@@ -198,6 +200,12 @@ def attn_bwd_noalloc(q, k, v, do, lse, delta, dq, dk, dv, *, causal: bool, scale
     _check(st, "pfa_attn_bwd_noalloc")
 
 
+def wait_probe(stream=None) -> None:
+    """pfa_wait_probe: enqueue the bounded-wait self-test (sets PFA_DEVERR_TIMEOUT after
+    about a second; see include/pfa.h)."""
+    _check(load().pfa_wait_probe(_stream(stream)), "pfa_wait_probe")
+
+
 def device_error(clear: bool = False) -> int:
     """pfa_device_error: the PFA_DEVERR_* bits of the current device (synchronises)."""
     st = load().pfa_device_error(int(bool(clear)))
@@ -213,6 +221,6 @@ def device_error_site() -> dict | None:
         raise PfaError(w, "pfa_device_error_site")
     if w == 0:
         return None
-    return {"kernel": {1: "forward", 2: "backward", 3: "delta_alt"}.get((w >> 56) & 15, "?"),
+    return {"kernel": {1: "forward", 2: "backward", 3: "delta_alt", 4: "wait_probe"}.get((w >> 56) & 15, "?"),
             "drain": bool((w >> 55) & 1), "parity": (w >> 54) & 1,
             "barrier_offset": (w >> 32) & 0x3FFFFF, "block": w & 0xFFFFFFFF}

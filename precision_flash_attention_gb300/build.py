@@ -23,7 +23,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpfa.so")
 STAMP = os.path.join(BUILD_DIR, "stamp.txt")
 
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_delta.cu", "attn_bwd_noalloc.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_delta.cu", "attn_bwd_noalloc.cu",
+           "wait_probe.cu"]
 HEADERS = [os.path.join(CSRC, "pfa_device.cuh"), os.path.join(CSRC, "pfa_internal.h"),
            os.path.join(INCLUDE, "pfa.h")]
 

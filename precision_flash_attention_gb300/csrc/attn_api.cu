@@ -340,6 +340,13 @@ int pfa_device_error(int clear) {
   return word;
 }
 
+int pfa_wait_probe(pfa_stream_t stream) {
+  DeviceState* dev = nullptr;
+  const int rc = current_device(&dev);
+  if (rc != PFA_OK) return rc;
+  return launched(pfa::launch_wait_probe(dev->err, dev->site, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 long long pfa_device_error_site(void) {
   DeviceState* dev = nullptr;
   int rc = current_device(&dev);

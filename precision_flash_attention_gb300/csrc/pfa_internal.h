@@ -87,5 +87,8 @@ cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cuda
 // Zeroes n4 float4 values of the dQ workspace on `stream` (a kernel, so that it
 // overlaps its neighbours by programmatic dependent launch).
 cudaError_t launch_zero_workspace(float* ws, long long n4, cudaStream_t stream);
+// One warp whose bounded wait on an mbarrier that nothing completes gives up
+// (PFA_DEVERR_TIMEOUT, error site kernel id 4).
+cudaError_t launch_wait_probe(int* err, unsigned long long* site, cudaStream_t stream);
 
 }  // namespace pfa
