@@ -1,7 +1,8 @@
 """CPU oracle for stabilised BF16 flash attention (forward and backward).
 
 TEST INFRASTRUCTURE, not part of the product. Only ``tests/``,
-``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+``__graft_entry__.smoke()``, and ``bench.py``'s CPU-baseline leg and its
+``--impl reference`` arm (both time the oracle on the host cores) may
 import, call or execute anything in this package. The CUDA path never imports
 it and it never imports the CUDA path; the two share no code, header, helper,
 table or constant. The only shared module is the seeded input generator
