@@ -129,7 +129,8 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
                  pfa_stream_t stream);
 
 /* The backward kernel alone, accumulating dQ in FP32 (no counterpart in the
- * paper): dq_accum += alpha dS K, and dK, dV (BF16) are written, with the same
+ * paper): dq_accum += dS K (dS = alpha P o (dP - delta) as above, so alpha
+ * enters once), and dK, dV (BF16) are written, with the same
  * arguments, equations and checks as pfa_attn_bwd. dq_accum is [B, H_q, N, d]
  * FP32, caller-owned device memory, 16-byte aligned; it is neither zeroed nor
  * converted. For gradient accumulation across calls (micro-batches or chunks of

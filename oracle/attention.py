@@ -37,8 +37,9 @@ Two precisions:
   accumulation: each dot product is formed exactly and rounded once to FP32
   (an order-free stand-in for an FP32 accumulator); Pbar is computed in FP32,
   rounded to BF16 and flushed to zero below the FP32 normal range; l sums the
-  BF16 Pbar; O, dQ, dK, dV are rounded to BF16 at the end; P and dS are rounded
-  to BF16 before the products they feed.
+  FP32 Pbar (before its BF16 cast, which only the Pbar V product sees); O, dQ,
+  dK, dV are rounded to BF16 at the end; P and dS are rounded to BF16 before the
+  products they feed.
 
 Diagnostic counters (per call, summed over all rows): ``repeated_rows`` =
 number of repeated rows; ``ones`` = number of entries whose BF16 Pbar under

@@ -93,11 +93,62 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _bhnd(t: torch.Tensor, name: str, dtype=torch.bfloat16, ndim=4) -> None:
-    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _layout(t, name: str, dtype=torch.bfloat16, ndim=4) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch tensor")
     if t.dtype != dtype or t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-d {dtype} tensor")
+
+
+def _dims(q, k) -> tuple:
+    """(B, H_q, H_kv, N, d) from q [B, H_q, N, d] and k [B, H_kv, N, d]."""
+    B, Hq, N, d = q.shape
+    if k.shape[0] != B or k.shape[2] != N or k.shape[3] != d:
+        raise ValueError(f"k has shape {tuple(k.shape)}: expected [B, H_kv, N, d] with q's "
+                         f"B={B}, N={N}, d={d}")
+    Hkv = k.shape[1]
+    if Hkv < 1 or Hq % Hkv != 0:
+        raise ValueError(f"H_q={Hq} must be a multiple of H_kv={Hkv}")
+    return B, Hq, Hkv, N, d
+
+
+def _expect(t, name: str, shape) -> None:
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _on_device(*named) -> None:
+    """Every tensor is a CUDA tensor on the current device (the one the call launches on)."""
+    for t, name in named:
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    for t, name in named:
+        if t.device.index != cur:
+            raise ValueError(f"{name} is on cuda:{t.device.index}, but the current device is "
+                             f"cuda:{cur}")
+
+
+def _check_qkv(q, k, v, extra_q=(), extra_k=(), rows=(), also=()) -> tuple:
+    """Layout, shape and device checks shared by the wrappers: q-shaped and k-shaped BF16
+    tensors, [B, H_q, N] FP32 row tensors, and ``also``: (tensor, name) pairs whose own
+    layout and shape the caller has checked, included in the device check. Raises
+    ValueError before anything is launched; shapes are checked before devices."""
+    named_q = [(q, "q")] + list(extra_q)
+    named_k = [(k, "k"), (v, "v")] + list(extra_k)
+    for t, n in named_q + named_k:
+        _layout(t, n)
+    for t, n in rows:
+        _layout(t, n, torch.float32, 3)
+    B, Hq, Hkv, N, d = _dims(q, k)
+    for t, n in named_q:
+        _expect(t, n, (B, Hq, N, d))
+    for t, n in named_k:
+        _expect(t, n, (B, Hkv, N, d))
+    for t, n in rows:
+        _expect(t, n, (B, Hq, N))
+    _on_device(*(named_q + named_k + list(rows) + list(also)))
+    return B, Hq, Hkv, N, d
 
 
 def _ptr(t):
@@ -107,15 +158,14 @@ def _ptr(t):
 def attn_fwd(q, k, v, o, lse, *, causal: bool, scale: float, fix_mode: int = 0,
              beta: float = 2.0, eps: float = 1e-3, counters=None, stream=None) -> None:
     """pfa_attn_fwd: O and lse of stabilised attention (see include/pfa.h)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
-        _bhnd(t, n)
-    _bhnd(lse, "lse", torch.float32, 3)
+    also = []
     if counters is not None:
-        _bhnd(counters, "counters", torch.int64, 1)
+        _layout(counters, "counters", torch.int64, 1)
         if counters.numel() != 3:
             raise ValueError("counters must hold 3 int64 values")
-    B, Hq, N, d = q.shape
-    st = load().pfa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, k.shape[1], N,
+        also = [(counters, "counters")]
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(o, "o")], rows=[(lse, "lse")], also=also)
+    st = load().pfa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N,
                              d, int(bool(causal)), float(scale), int(fix_mode), float(beta),
                              float(eps), _ptr(counters) if counters is not None else None,
                              _stream(stream))
@@ -124,23 +174,23 @@ def attn_fwd(q, k, v, o, lse, *, causal: bool, scale: float, fix_mode: int = 0,
 
 def attn_delta(o, do, delta, *, stream=None) -> None:
     """pfa_attn_delta: delta = rowsum(dO o O)."""
-    _bhnd(o, "o")
-    _bhnd(do, "do")
-    _bhnd(delta, "delta", torch.float32, 3)
+    _layout(o, "o")
+    _layout(do, "do")
+    _layout(delta, "delta", torch.float32, 3)
     B, Hq, N, d = o.shape
+    _expect(do, "do", o.shape)
+    _expect(delta, "delta", (B, Hq, N))
+    _on_device((o, "o"), (do, "do"), (delta, "delta"))
     st = load().pfa_attn_delta(_ptr(o), _ptr(do), _ptr(delta), B, Hq, N, d, _stream(stream))
     _check(st, "pfa_attn_delta")
 
 
 def attn_delta_alt(q, k, v, do, lse, delta, *, causal: bool, scale: float, stream=None) -> None:
     """pfa_attn_delta_alt: delta = rowsum(dP o P) with P, dP recomputed."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do")):
-        _bhnd(t, n)
-    _bhnd(lse, "lse", torch.float32, 3)
-    _bhnd(delta, "delta", torch.float32, 3)
-    B, Hq, N, d = q.shape
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do")],
+                                  rows=[(lse, "lse"), (delta, "delta")])
     st = load().pfa_attn_delta_alt(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta), B,
-                                   Hq, k.shape[1], N, d, int(bool(causal)), float(scale),
+                                   Hq, Hkv, N, d, int(bool(causal)), float(scale),
                                    _stream(stream))
     _check(st, "pfa_attn_delta_alt")
 
@@ -152,34 +202,30 @@ def bwd_workspace_bytes(B: int, H_q: int, N: int, d: int) -> int:
 def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, scale: float,
              stream=None) -> None:
     """pfa_attn_bwd: dQ, dK, dV from lse and delta (dq_accum is the FP32 workspace)."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _bhnd(t, n)
-    _bhnd(lse, "lse", torch.float32, 3)
-    _bhnd(delta, "delta", torch.float32, 3)
-    if dq_accum.device.type != "cuda" or dq_accum.dtype != torch.float32 or not dq_accum.is_contiguous():
-        raise ValueError("dq_accum must be a contiguous float32 CUDA tensor")
-    B, Hq, N, d = q.shape
-    if dq_accum.numel() * 4 < bwd_workspace_bytes(B, Hq, N, d):
+    if (not isinstance(dq_accum, torch.Tensor) or dq_accum.dtype != torch.float32
+            or not dq_accum.is_contiguous()):
+        raise ValueError("dq_accum must be a contiguous float32 tensor")
+    if q.dim() == 4 and dq_accum.numel() < q.numel():
         raise ValueError("dq_accum is smaller than bwd_workspace_bytes()")
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do"), (dq, "dq")],
+                                  extra_k=[(dk, "dk"), (dv, "dv")],
+                                  rows=[(lse, "lse"), (delta, "delta")], also=[(dq_accum, "dq_accum")])
     st = load().pfa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta), _ptr(dq),
-                             _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, k.shape[1], N, d,
+                             _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, Hkv, N, d,
                              int(bool(causal)), float(scale), _stream(stream))
     _check(st, "pfa_attn_bwd")
 
 
 def attn_bwd_accum(q, k, v, do, lse, delta, dq_accum, dk, dv, *, causal: bool, scale: float,
                    stream=None) -> None:
-    """pfa_attn_bwd_accum: dq_accum (FP32 [B, H_q, N, d]) += alpha dS K; dk, dv written."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do"), (dk, "dk"), (dv, "dv")):
-        _bhnd(t, n)
-    _bhnd(lse, "lse", torch.float32, 3)
-    _bhnd(delta, "delta", torch.float32, 3)
-    _bhnd(dq_accum, "dq_accum", torch.float32)
-    B, Hq, N, d = q.shape
-    if dq_accum.shape != q.shape:
-        raise ValueError("dq_accum must have the shape of q")
+    """pfa_attn_bwd_accum: dq_accum (FP32 [B, H_q, N, d]) += dS K; dk, dv written."""
+    _layout(dq_accum, "dq_accum", torch.float32)
+    _layout(q, "q")
+    _expect(dq_accum, "dq_accum", q.shape)
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do")], extra_k=[(dk, "dk"), (dv, "dv")],
+                                  rows=[(lse, "lse"), (delta, "delta")], also=[(dq_accum, "dq_accum")])
     st = load().pfa_attn_bwd_accum(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
-                                   _ptr(dq_accum), _ptr(dk), _ptr(dv), B, Hq, k.shape[1], N, d,
+                                   _ptr(dq_accum), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
                                    int(bool(causal)), float(scale), _stream(stream))
     _check(st, "pfa_attn_bwd_accum")
 
@@ -189,13 +235,11 @@ def attn_bwd_noalloc(q, k, v, do, lse, delta, dq, dk, dv, *, causal: bool, scale
     """pfa_attn_bwd_noalloc: the backward pass without a caller workspace, for callers that
     may not allocate device memory; its dQ accumulation buffer is a fixed library-owned array
     (B * H_q * N * d <= 8,388,608), shared by all calls on a device."""
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (do, "do"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
-        _bhnd(t, n)
-    _bhnd(lse, "lse", torch.float32, 3)
-    _bhnd(delta, "delta", torch.float32, 3)
-    B, Hq, N, d = q.shape
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do"), (dq, "dq")],
+                                  extra_k=[(dk, "dk"), (dv, "dv")],
+                                  rows=[(lse, "lse"), (delta, "delta")])
     st = load().pfa_attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
-                                     _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, k.shape[1], N, d,
+                                     _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d,
                                      int(bool(causal)), float(scale), _stream(stream))
     _check(st, "pfa_attn_bwd_noalloc")
 

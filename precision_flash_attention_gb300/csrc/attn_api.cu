@@ -21,49 +21,98 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr double kRoundToOneWindow = 1.9550348e-3;
 
 struct DeviceState {
-  bool ready = false;
+  bool checked = false;
   bool supported = false;
-  int* err = nullptr;  // device address of g_pfa_device_error on this device
+  unsigned long long ctx = 0;  // id of the context the addresses below belong to (0: none yet)
+  int* err = nullptr;  // device address of g_pfa_device_error in that context
   unsigned long long* site = nullptr;  // device address of g_pfa_device_error_site
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-bool g_encode_tried = false;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+bool g_entry_points_tried = false;
 
-// Looks up (once per device, with that device current) whether it is an sm_103
-// part and where the error word lives.
-int current_device(DeviceState** out) {
+// The most recent CUDA error seen by this thread's calls into the library.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+// Driver entry points, looked up once (the caller holds g_mu).
+void load_entry_points() {
+  if (g_entry_points_tried) return;
+  g_entry_points_tried = true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+          cudaSuccess && q == cudaDriverEntryPointSuccess)
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+  cudaGetLastError();  // a failed lookup leaves nothing pending
+}
+
+// Whether the current device is an sm_103 part (looked up once per device; the
+// caller holds g_mu).
+int check_device_locked(int* dev_out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PFA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
-  DeviceState& st = g_dev[dev];
-  if (!st.ready) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return PFA_ERR_LAUNCH;
-    st.supported = (major == 10 && minor == 3);
-    if (st.supported) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_pfa_device_error) != cudaSuccess) return PFA_ERR_LAUNCH;
-      st.err = static_cast<int*>(p);
-      if (cudaGetSymbolAddress(&p, g_pfa_device_error_site) != cudaSuccess) return PFA_ERR_LAUNCH;
-      st.site = static_cast<unsigned long long*>(p);
-    }
-    if (!g_encode_tried) {
-      g_encode_tried = true;
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q) == cudaSuccess &&
-          q == cudaDriverEntryPointSuccess)
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    st.ready = true;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return PFA_ERR_UNSUPPORTED;
   }
-  if (!st.supported || g_encode == nullptr) return PFA_ERR_UNSUPPORTED;
+  DeviceState& st = g_dev[dev];
+  if (!st.checked) {
+    int major = 0, minor = 0;
+    const cudaError_t e1 = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    const cudaError_t e2 = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e1 != cudaSuccess || e2 != cudaSuccess) {
+      g_last_cuda_error = e1 != cudaSuccess ? e1 : e2;
+      cudaGetLastError();
+      return PFA_ERR_LAUNCH;
+    }
+    st.supported = (major == 10 && minor == 3);
+    st.checked = true;
+  }
+  load_entry_points();
+  if (!st.supported || g_encode == nullptr || g_ctx_current == nullptr || g_ctx_get_id == nullptr)
+    return PFA_ERR_UNSUPPORTED;
+  *dev_out = dev;
+  return PFA_OK;
+}
+
+// Looks up, with the device current, whether it is an sm_103 part and where the
+// error words live. Module symbols have one address per CUDA context, so the
+// addresses are looked up again whenever the thread's current context is not
+// the one they were taken in (a caller's own driver context, or a primary
+// context created anew after cudaDeviceReset).
+int current_device(DeviceState** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  int rc = check_device_locked(&dev);
+  if (rc != PFA_OK) return rc;
+  DeviceState& st = g_dev[dev];
+  unsigned long long id = 0;
+  if ((rc = pfa::context_id(&id)) != PFA_OK) return rc;
+  if (id == 0 || id != st.ctx) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_pfa_device_error);
+    void* p2 = nullptr;
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&p2, g_pfa_device_error_site);
+    if (e != cudaSuccess) {
+      g_last_cuda_error = e;
+      cudaGetLastError();
+      return PFA_ERR_LAUNCH;
+    }
+    // The lookup created the primary context if none was current.
+    if ((rc = pfa::context_id(&id)) != PFA_OK) return rc;
+    st.err = static_cast<int*>(p);
+    st.site = static_cast<unsigned long long*>(p2);
+    st.ctx = id;
+  }
   *out = &st;
   return PFA_OK;
 }
@@ -125,9 +174,6 @@ pfa::AttnShape shape(int B, int Hq, int Hkv, int N, int d, int causal, float sca
   return s;
 }
 
-// The most recent CUDA error seen by this thread's calls into the library.
-thread_local cudaError_t g_last_cuda_error = cudaSuccess;
-
 int launched(cudaError_t e) {
   if (e == cudaSuccess) return PFA_OK;
   g_last_cuda_error = e;
@@ -135,6 +181,31 @@ int launched(cudaError_t e) {
 }
 
 }  // namespace
+
+namespace pfa {
+
+int context_id(unsigned long long* id) {
+  *id = 0;
+  if (g_ctx_current == nullptr || g_ctx_get_id == nullptr) return PFA_ERR_UNSUPPORTED;
+  CUcontext ctx = nullptr;
+  if (g_ctx_current(&ctx) != CUDA_SUCCESS) return PFA_ERR_LAUNCH;
+  if (ctx == nullptr) return PFA_OK;  // no context current yet
+  return g_ctx_get_id(ctx, id) == CUDA_SUCCESS ? PFA_OK : PFA_ERR_LAUNCH;
+}
+
+int check_device() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev = 0;
+  return check_device_locked(&dev);
+}
+
+void note_cuda_error(cudaError_t e) {
+  if (e == cudaSuccess) return;
+  g_last_cuda_error = e;
+  cudaGetLastError();
+}
+
+}  // namespace pfa
 
 extern "C" {
 

@@ -20,25 +20,46 @@ constexpr size_t kNoallocMaxElems = size_t(1) << 23;  // 8,388,608 values = 32 M
 
 // One array per device, created when the library's device code is loaded. In
 // host code this name only stands in for the symbol: its device address must be
-// looked up with cudaGetSymbolAddress on each device.
+// looked up with cudaGetSymbolAddress, with the device current.
 static __device__ __align__(256) float g_bwd_dq_scratch[kNoallocMaxElems];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
-float* g_scratch_addr[kMaxDevices] = {};
+// The array's address per device, and the id of the CUDA context it was taken in:
+// a symbol has one address per context, so a call from another context (a
+// caller's own driver context, or a primary context created anew after
+// cudaDeviceReset) looks it up again.
+struct ScratchAddr {
+  unsigned long long ctx = 0;
+  float* ptr = nullptr;
+};
+ScratchAddr g_scratch[kMaxDevices];
 
-// Device address of the array on the current device, looked up once per device.
 int scratch_on_current_device(float** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PFA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_dq_scratch) != cudaSuccess || p == nullptr)
-      return PFA_ERR_LAUNCH;
-    g_scratch_addr[dev] = static_cast<float*>(p);
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    pfa::note_cuda_error(ge);
+    return PFA_ERR_UNSUPPORTED;
   }
-  *out = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  unsigned long long id = 0;
+  int rc = pfa::context_id(&id);
+  if (rc != PFA_OK) return rc;
+  ScratchAddr& s = g_scratch[dev];
+  if (id == 0 || id != s.ctx || s.ptr == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_dq_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      pfa::note_cuda_error(e);
+      return PFA_ERR_LAUNCH;
+    }
+    // The lookup created the primary context if none was current.
+    if ((rc = pfa::context_id(&id)) != PFA_OK) return rc;
+    s.ptr = static_cast<float*>(p);
+    s.ctx = id;
+  }
+  *out = s.ptr;
   return PFA_OK;
 }
 
@@ -52,9 +73,11 @@ extern "C" int pfa_attn_bwd_noalloc(const pfa_bf16* q, const pfa_bf16* k, const 
   const size_t need = pfa_bwd_workspace_bytes(B, H_q, N, d);
   if (need == 0) return PFA_ERR_INVALID_ARG;
   if (need > kNoallocMaxElems * sizeof(float)) return PFA_ERR_TOO_LARGE;
-  float* scratch = nullptr;
-  const int rc = scratch_on_current_device(&scratch);
+  // An unsupported device is reported as such before the symbol lookup.
+  int rc = pfa::check_device();
   if (rc != PFA_OK) return rc;
+  float* scratch = nullptr;
+  if ((rc = scratch_on_current_device(&scratch)) != PFA_OK) return rc;
   // pfa_attn_bwd zeroes the buffer on `stream` before its kernels accumulate into it.
   return pfa_attn_bwd(q, k, v, dO, lse, delta, dq, dk, dv, scratch, B, H_q, H_kv, N, d, causal,
                       scale, stream);

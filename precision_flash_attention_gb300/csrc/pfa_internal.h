@@ -28,6 +28,16 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Identity (cuCtxGetId) of the CUDA context current on the calling thread; 0 when
+// none is current yet. Module symbols have one device address per context.
+int context_id(unsigned long long* id);
+// PFA_OK if the current device is an sm_103 part and the driver entry points the
+// library needs are present; PFA_ERR_UNSUPPORTED (or PFA_ERR_LAUNCH) otherwise.
+int check_device();
+// Records a CUDA error for pfa_last_error() on this thread and clears it from
+// the runtime, so that it is not reported again by a later call.
+void note_cuda_error(cudaError_t e);
+
 constexpr int kTile = 128;  // rows of a Q tile and of a K/V tile
 
 // Arguments common to the tiled kernels (all sizes in elements).

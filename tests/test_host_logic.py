@@ -49,3 +49,43 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["config"]["N"] == 1024 and line["config"]["d"] == 64
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_binding_rejects_mismatched_shapes_before_any_launch():
+    # The wrappers check every tensor's shape against q and k before they look at devices or
+    # call into the library, so these CPU tensors never reach a kernel.
+    import pytest
+    import torch
+
+    from precision_flash_attention_gb300 import _lib
+
+    bf = lambda *s: torch.zeros(s, dtype=torch.bfloat16)  # noqa: E731
+    f32 = lambda *s: torch.zeros(s, dtype=torch.float32)  # noqa: E731
+    q, k, v, do = bf(2, 4, 64, 64), bf(2, 2, 64, 64), bf(2, 2, 64, 64), bf(2, 4, 64, 64)
+    lse, delta = f32(2, 4, 64), f32(2, 4, 64)
+    dq, dk, dv = bf(2, 4, 64, 64), bf(2, 2, 64, 64), bf(2, 2, 64, 64)
+    kw = dict(causal=True, scale=0.125)
+    cases = [
+        (dict(dq=bf(2, 4, 32, 64)), "dq"),          # dq smaller than q
+        (dict(dk=bf(2, 4, 64, 64)), "dk"),          # dk shaped like q, not like k
+        (dict(dv=bf(2, 2, 64, 32)), "dv"),
+        (dict(lse=f32(2, 4, 63)), "lse"),
+        (dict(delta=f32(2, 2, 64)), "delta"),
+        (dict(k=bf(2, 3, 64, 64), v=bf(2, 3, 64, 64)), "multiple"),  # H_kv does not divide H_q
+        (dict(v=bf(2, 2, 65, 64)), "v"),
+    ]
+    for change, what in cases:
+        a = dict(q=q, k=k, v=v, do=do, lse=lse, delta=delta, dq=dq, dk=dk, dv=dv)
+        a.update(change)
+        with pytest.raises(ValueError, match=what):
+            _lib.attn_bwd_noalloc(a["q"], a["k"], a["v"], a["do"], a["lse"], a["delta"], a["dq"],
+                                  a["dk"], a["dv"], **kw)
+    with pytest.raises(ValueError, match="o has shape"):
+        _lib.attn_fwd(q, k, v, bf(2, 4, 64, 128), lse, **kw)
+    with pytest.raises(ValueError, match="delta"):
+        _lib.attn_delta(q, do, f32(2, 4, 32))
+    with pytest.raises(ValueError, match="dq_accum"):
+        _lib.attn_bwd_accum(q, k, v, do, lse, delta, f32(2, 4, 64, 32), dk, dv, **kw)
+    # Shapes that agree get as far as the device check (CPU tensors are refused there).
+    with pytest.raises(ValueError, match="CUDA"):
+        _lib.attn_bwd_noalloc(q, k, v, do, lse, delta, dq, dk, dv, **kw)

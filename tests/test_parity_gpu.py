@@ -306,7 +306,7 @@ def test_stream_and_autograd_wrapper():
 
 @pytest.mark.parametrize("shape", [(1, 4, 2, 300, 64), (1, 2, 1, 200, 128)], ids=["d64-gqa", "d128"])
 def test_bwd_accumulate_entry_point(shape):
-    # pfa_attn_bwd_accum adds alpha dS K into a caller's FP32 buffer and writes dK, dV;
+    # pfa_attn_bwd_accum adds dS K (alpha is inside dS) into a caller's FP32 buffer and writes dK, dV;
     # two calls on one buffer give twice dQ, and dK, dV match pfa_attn_bwd.
     B, Hq, Hkv, N, d = shape
     t = to_dev(inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.5, std_do=1.0, seed=7))

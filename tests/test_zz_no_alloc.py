@@ -61,6 +61,27 @@ def test_noalloc_matches_workspace_entry_point(pfa, shape):
     assert pfa.device_error() == 0
 
 
+def test_noalloc_python_wrapper(pfa):
+    # The same entry point through the package's binding, which checks shapes and devices.
+    from precision_flash_attention_gb300 import inputs
+    t = {n: x.cuda() for n, x in inputs.gaussian(1, 4, 2, 200, 64, std_qkv=0.5, std_do=1e-2,
+                                                  seed=3).items()}
+    o, lse = pfa.forward(t["q"], t["k"], t["v"], causal=True, scale=0.125, fix_mode=2)
+    dq_ref, dk_ref, dv_ref, delta = pfa.backward(t["q"], t["k"], t["v"], o, lse, t["do"],
+                                                 causal=True, scale=0.125)
+    for _ in range(2):
+        dq, dk, dv = (torch.full_like(x, float("nan")) for x in (t["q"], t["k"], t["v"]))
+        pfa.attn_bwd_noalloc(t["q"], t["k"], t["v"], t["do"], lse, delta, dq, dk, dv, causal=True,
+                             scale=0.125)
+        torch.cuda.synchronize()
+        for got, ref in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+            assert _rel(got, ref) <= TOL
+    with pytest.raises(ValueError):
+        pfa.attn_bwd_noalloc(t["q"], t["k"], t["v"], t["do"], lse[:, :, :100].contiguous(), delta,
+                             dq, dk, dv, causal=True, scale=0.125)
+    assert pfa.device_error() == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_buffer(pfa):
     # 8 * 16 * 8192 * 128 = 134M values > 8,388,608: refused before anything is launched.
     lib = pfa.load()
