@@ -38,8 +38,12 @@ Two precisions:
   (an order-free stand-in for an FP32 accumulator); Pbar is computed in FP32,
   rounded to BF16 and flushed to zero below the FP32 normal range; l sums the
   FP32 Pbar (before its BF16 cast, which only the Pbar V product sees); O, dQ,
-  dK, dV are rounded to BF16 at the end; P and dS are rounded to BF16 before the
-  products they feed.
+  dK, dV are rounded to BF16 at the end. In the backward pass P = exp(S - lse)
+  is FP32 (flushed to zero below the normal range), dS = P o (dP - delta) is
+  formed in FP32 and, like P, rounded to BF16 before the products it feeds;
+  alpha multiplies the FP32 results of the dQ and dK products (so the BF16 dS
+  does not carry it). The pages fix the equation dS = alpha P o (dP - delta)
+  but no rounding points; these are the backward kernel's.
 
 Diagnostic counters (per call, summed over all rows): ``repeated_rows`` =
 number of repeated rows; ``ones`` = number of entries whose BF16 Pbar under
@@ -272,16 +276,19 @@ def attn_bwd(q, k, v, do, lse, delta, *, causal=False, scale=None, emulate_bf16=
             dp = do[b, h] @ v[b, kv].T
             dlt = np.asarray(delta[b, h], dtype=np.float64)[:, None]
             if emulate_bf16:
+                # P o (dP - delta) in FP32 and cast to BF16 as the dQ / dK operand; alpha
+                # multiplies the FP32 products afterwards, where the kernel applies it.
                 dp = fp32(dp).astype(np.float64)
-                ds = fp32(fp32(p * fp32(dp - dlt)) * np.float32(scale)).astype(np.float64)
+                ds_op = bf16_rne(fp32(p * fp32(dp - dlt))).astype(np.float64)
                 p_op = bf16_rne(fp32(p)).astype(np.float64)
-                ds_op = bf16_rne(fp32(ds)).astype(np.float64)
             else:
-                ds = scale * p * (dp - dlt)
-                p_op, ds_op = p, ds
+                ds_op = scale * p * (dp - dlt)
+                p_op = p
             dq[b, h] = ds_op @ k[b, kv]
             dk[b, kv] += ds_op.T @ q[b, h]
             dv[b, kv] += p_op.T @ do[b, h]
     if emulate_bf16:
-        dq, dk, dv = (bf16_rne(fp32(x)).astype(np.float64) for x in (dq, dk, dv))
+        a32 = np.float32(scale)
+        dq, dk = (bf16_rne(fp32(fp32(x) * a32)).astype(np.float64) for x in (dq, dk))
+        dv = bf16_rne(fp32(dv)).astype(np.float64)
     return {"dq": dq, "dk": dk, "dv": dv}
