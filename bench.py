@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -28,6 +29,8 @@ import torch  # noqa: E402
 METRIC = "attention fwd+bwd TFLOP/s and % of GB300 BF16 peak (GPT-2 shape, N=1k–8k)"
 WORKLOAD = dict(B=8, H=12, N=1024, d=64, causal=True, scale=0.125, beta=2.0, eps=1e-3)
 L2_FLUSH_BYTES = 256 << 20
+# The timed region spans at least this long, so the clock record holds several samples.
+TIMED_REGION_MIN_S = 0.06
 # Kernels of ours launched per step: attn_fwd, delta, the dQ workspace zeroing,
 # attn_bwd and the dQ conversion.
 LAUNCHES_PER_STEP = 5
@@ -236,9 +239,10 @@ def make_inputs(device, B, H, N, d, seed=0):
 
 
 class Step:
-    """Buffers and launch sequence of one forward + backward step."""
+    """Buffers and launch sequence of one forward + backward step (GQA when k has fewer heads
+    than q). ``delta_mode`` 0 takes delta = rowsum(dO o O), 1 delta = rowsum(dP o P)."""
 
-    def __init__(self, t, *, causal, scale, fix_mode, beta, eps):
+    def __init__(self, t, *, causal, scale, fix_mode, beta, eps, delta_mode=0):
         import precision_flash_attention_gb300 as pfa
         self.pfa = pfa
         self.t = t
@@ -246,9 +250,11 @@ class Step:
         B, H, N, d = q.shape
         self.kw = dict(causal=causal, scale=scale)
         self.fkw = dict(fix_mode=fix_mode, beta=beta, eps=eps)
+        self.delta_mode = delta_mode
         self.o = torch.empty_like(q)
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
         self.delta = torch.empty_like(self.lse)
+        self.delta_alt = torch.empty_like(self.lse)
         self.dq, self.dk, self.dv = (torch.empty_like(t[n]) for n in ("q", "k", "v"))
         self.ws = torch.empty(pfa.bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
                               device=q.device)
@@ -258,7 +264,15 @@ class Step:
         self.pfa.attn_fwd(t["q"], t["k"], t["v"], self.o, self.lse, **self.kw, **self.fkw)
 
     def delta_(self):
-        self.pfa.attn_delta(self.o, self.t["do"], self.delta)
+        if self.delta_mode == 0:
+            self.pfa.attn_delta(self.o, self.t["do"], self.delta)
+        else:
+            self.delta_alt_(self.delta)
+
+    def delta_alt_(self, out=None):
+        t = self.t
+        self.pfa.attn_delta_alt(t["q"], t["k"], t["v"], t["do"], self.lse,
+                                self.delta_alt if out is None else out, **self.kw)
 
     def bwd(self):
         t = self.t
@@ -281,7 +295,8 @@ def time_step(step, steps, warmup, flush, split=False):
     """CUDA-event timing of whole steps on the launching stream; L2 flushed before each
     step. The kernels of a step overlap their neighbours (programmatic dependent launch),
     so events go only at the step's ends; with `split` they also go between the calls,
-    which serialises them, to give each call's own duration."""
+    which serialises them, to give each call's own duration (and the backward kernel, and
+    delta = rowsum(dP o P), each timed by itself)."""
     for _ in range(warmup):
         flush.fill_(1.0)
         step.run()
@@ -306,20 +321,83 @@ def time_step(step, steps, warmup, flush, split=False):
         out.update(fwd_ms=[a[0].elapsed_time(a[1]) for a in rec],
                    delta_ms=[a[1].elapsed_time(a[2]) for a in rec],
                    bwd_ms=[a[2].elapsed_time(a[3]) for a in rec])
-        # The backward kernel by itself: its workspace zeroed and L2 flushed outside
-        # the events.
-        kr = []
-        for _ in range(steps):
-            flush.fill_(1.0)
-            step.ws.zero_()
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            e[0].record()
-            step.bwd_kernel()
-            e[1].record()
-            kr.append(e)
-        torch.cuda.synchronize()
-        out["bwd_kernel_ms"] = [a[0].elapsed_time(a[1]) for a in kr]
+
+        def alone(fn, before=None):
+            # One call by itself: L2 flushed (and `before` run) outside the events.
+            kr = []
+            for _ in range(steps):
+                flush.fill_(1.0)
+                if before is not None:
+                    before()
+                e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                e[0].record()
+                fn()
+                e[1].record()
+                kr.append(e)
+            torch.cuda.synchronize()
+            return [a[0].elapsed_time(a[1]) for a in kr]
+
+        out["bwd_kernel_ms"] = alone(step.bwd_kernel, step.ws.zero_)
+        out["delta_alt_ms"] = alone(step.delta_alt_)
     return out
+
+
+# The other configured workloads, each timed in every mode it lists (tests check them against
+# the oracle; here they are measured). Mode 2 is added for the GPT-2 layer.
+OTHER_WORKLOADS = [
+    ("tiny", "C1 tiny: B=1 H=1 N=64 d=64 non-causal"),
+    ("gpt2", "C2 GPT-2-small layer: B=8 H=12 N=1024 d=64 causal (all three modes)"),
+    ("sink", "C3 sink-heavy: B=4 H=12 N=2048 d=64 causal, delta = rowsum(dP o P)"),
+    ("long", "C4 long context: B=2 H=16 N=8192 d=128 causal, beta=4"),
+    ("gqa", "C5 Llama-3.1-8B-style GQA: B=1 H_q=32 H_kv=8 N=8192 d=128 causal"),
+]
+
+
+def measure_workload(name, device, steps, flush, peaks):
+    """fwd, delta, delta-alt, bwd and whole-step timings of one named workload (inputs from
+    precision_flash_attention_gb300.inputs) in each of its modes, with algorithmic TFLOP/s
+    and fractions of the measured peaks. The sink-heavy step takes delta = rowsum(dP o P)
+    (the variant its parity test uses); delta = rowsum(dO o O) is timed too."""
+    from precision_flash_attention_gb300 import inputs
+    wl = inputs.WORKLOADS[name]
+    t = {n: x.to(device) for n, x in inputs.make(name, seed=0).items()}
+    B, Hq, N, d = t["q"].shape
+    modes = (0, 1, 2) if name == "gpt2" else wl.modes
+    peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
+    f_fwd, f_bwd, f_tot, f_alt = (wl.flops(w) for w in ("fwd", "bwd", "fwd+bwd", "delta_alt"))
+    dl_bytes = B * Hq * N * (4 * d + 4)
+    out = {}
+    for m in modes:
+        st = Step(t, causal=wl.causal, scale=wl.alpha, fix_mode=m, beta=wl.beta, eps=wl.eps,
+                  delta_mode=1 if name == "sink" else 0)
+        r = time_step(st, steps, 2, flush, split=True)
+        tot = time_step(st, steps, 0, flush)["step_ms"]
+        med = {k: statistics.median(v) for k, v in r.items()}
+        step_ms = statistics.median(tot)
+        e = {"fwd_ms": med["fwd_ms"], "bwd_call_ms": med["bwd_ms"], "bwd_kernel_ms": med["bwd_kernel_ms"],
+             "step_ms": step_ms,
+             "fwd_tflops": f_fwd / med["fwd_ms"] / 1e9,
+             "bwd_tflops": f_bwd / med["bwd_ms"] / 1e9,
+             "bwd_kernel_tflops": f_bwd / med["bwd_kernel_ms"] / 1e9,
+             "total_tflops": f_tot / step_ms / 1e9}
+        for k in ("fwd", "bwd", "bwd_kernel", "total"):
+            e[k + "_frac_bf16_peak"] = e[k + "_tflops"] / peak
+        e["delta_alt_ms"] = med["delta_alt_ms"]
+        e["delta_alt_tflops"] = f_alt / med["delta_alt_ms"] / 1e9
+        if name != "sink":
+            e["delta_ms"] = med["delta_ms"]
+            e["delta_gbs"] = dl_bytes / med["delta_ms"] / 1e6
+            e["delta_frac_hbm_peak"] = e["delta_gbs"] / hbm
+        else:
+            e["step_note"] = "step = fwd + delta_alt + bwd; total_tflops counts fwd+bwd FLOPs only"
+        out[f"mode {m}"] = e
+        del st
+    del t
+    torch.cuda.empty_cache()
+    return {"shape": dict(B=B, H_q=Hq, H_kv=wl.H_kv, N=N, d=d, causal=wl.causal, alpha=wl.alpha,
+                          beta=wl.beta, eps=wl.eps),
+            "flops": {"fwd": f_fwd, "bwd": f_bwd, "fwd+bwd": f_tot, "delta_alt": f_alt},
+            "delta_bytes": dl_bytes, "steps": steps, "modes": out}
 
 
 def e2e_time(make_step, steps, warmup):
@@ -433,8 +511,10 @@ def run_gpu_arm(args):
     t = make_inputs(dev, w["B"], w["H"], w["N"], w["d"], seed=rank)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     head = args.mode
+    # Modes 0, 1 and 2 interleaved in the timed region: the headline is `head` (1 by
+    # default), and the cost of each fix mode is read against mode 0 under the same load.
     steps = {m: Step(t, causal=w["causal"], scale=w["scale"], fix_mode=m, beta=w["beta"],
-                     eps=w["eps"]) for m in sorted({0, head})}
+                     eps=w["eps"]) for m in sorted({0, 1, 2, head})}
     # Clocks are sampled from before the warm-up (so sampling is live when timing
     # starts) until after an untimed tail of the same steps; not under ncu.
     clk = _NoClock() if args.kernels_only else ClockSampler(local)
@@ -448,19 +528,39 @@ def run_gpu_arm(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         # Interleave the modes so the cost of the fix is measured under the same conditions.
+        # One pass = K steps of each mode. The timed region repeats the pass until it spans
+        # several clock-sampling periods (a pass of the bench workload takes a few ms, less
+        # than one period); the line reports K and the number of passes.
+        def one_pass(res, log):
+            for it in range(args.steps):
+                for m in steps:
+                    r = time_step(steps[m], 1, 0, flush)
+                    for k2 in r:
+                        res[m][k2] += r[k2]
+                    if log and args.progress:
+                        err = pfa.device_error()
+                        _progress(args, f"step {it} mode {m}: {r['step_ms'][0]:.3f} ms, error word {err}"
+                                        + (f", first timeout at {pfa.device_error_site()}" if err else ""))
+            torch.cuda.synchronize()
+
+        passes = 1
+        if not args.kernels_only:
+            cal0 = time.perf_counter()
+            one_pass({m: {"step_ms": []} for m in steps}, False)
+            per_pass = time.perf_counter() - cal0
+            passes = max(1, min(50, math.ceil(TIMED_REGION_MIN_S / max(per_pass, 1e-6))))
+            if world > 1:
+                t_p = torch.tensor([passes], dtype=torch.int64, device=dev)
+                torch.distributed.all_reduce(t_p, op=torch.distributed.ReduceOp.MAX)
+                passes = int(t_p.item())
         res = {m: {"step_ms": []} for m in steps}
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
         clk.mark_start()
         wall0 = time.perf_counter()
-        for it in range(args.steps):
-            for m in steps:
-                r = time_step(steps[m], 1, 0, flush)
-                for k2 in r:
-                    res[m][k2] += r[k2]
-                if args.progress:
-                    err = pfa.device_error()
-                    _progress(args, f"step {it} mode {m}: {r['step_ms'][0]:.3f} ms, error word {err}"
-                                    + (f", first timeout at {pfa.device_error_site()}" if err else ""))
-        torch.cuda.synchronize()
+        for _ in range(passes):
+            one_pass(res, True)
         if world > 1:
             torch.distributed.barrier()
         wall = time.perf_counter() - wall0
@@ -518,24 +618,38 @@ def run_gpu_arm(args):
     mode_tflops = {str(m): f_total / (mean(r["step_ms"]) * 1e-3) / 1e12 for m, r in res.items()}
     overhead = (100.0 * (mean(res[head]["step_ms"]) / mean(res[0]["step_ms"]) - 1.0)
                 if head != 0 else None)
+    overhead_all = {str(m): 100.0 * (mean(res[m]["step_ms"]) / mean(res[0]["step_ms"]) - 1.0)
+                    for m in res if m != 0}
 
     sweep = {}
     _progress(args, f"timed steps done: {ms:.3f} ms per step")
     if args.sweep and rank == 0:
         for n_s in (2048, 4096, 8192):
             ts = make_inputs(dev, B, H, n_s, d, seed=1)
-            for m in sorted({0, head}):
+            tot_ms = {}
+            for m in (0, 1, 2):
                 _progress(args, f"sweep N={n_s} mode {m}")
                 st = Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
                 r = time_step(st, max(3, args.steps // 2), 2, flush, split=True)
-                fm, bm = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms"))
+                fm, bm, km = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms", "bwd_kernel_ms"))
                 sm = statistics.median(time_step(st, max(3, args.steps // 2), 0, flush)["step_ms"])
+                tot_ms[m] = sm
                 tot = flops(B, H, n_s, d, True) / sm / 1e9
                 sweep[f"N={n_s},mode={m}"] = {
                     "fwd_tflops": flops(B, H, n_s, d, True, "fwd") / fm / 1e9,
                     "bwd_tflops": flops(B, H, n_s, d, True, "bwd") / bm / 1e9,
+                    "bwd_kernel_tflops": flops(B, H, n_s, d, True, "bwd") / km / 1e9,
                     "total_tflops": tot, "total_frac_bf16_peak": tot / peak}
+                if m > 0:
+                    sweep[f"N={n_s},mode={m}"]["overhead_vs_mode0_pct"] = 100.0 * (sm / tot_ms[0] - 1.0)
+                del st
             del ts
+    workloads = {}
+    if args.sweep and rank == 0:
+        for name, label in OTHER_WORKLOADS:
+            _progress(args, f"workload {name}")
+            workloads[label] = measure_workload(name, dev, max(5, args.steps // 2), flush, peaks)
+        assert pfa.device_error() == 0, "device error word set while timing the workloads"
 
     _progress(args, f"sweep done, device error word {pfa.device_error()}")
     e2e = None
@@ -561,10 +675,11 @@ def run_gpu_arm(args):
         "data": "synthetic (seeded N(0,0.25) Q/K/V, N(0,1e-4) dO)",
         "config": dict(workload_config(world, head, w), l2="flushed (256 MiB write) before every step"),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(steps),
-        "clocks": clk.summary(), "wall_s_timed_region": wall,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps * len(steps) * passes,
+        "timed_passes": passes, "clocks": clk.summary(), "wall_s_timed_region": wall,
         "kernels": kernels, "mode_tflops": mode_tflops, "mode_overhead_pct": overhead,
-        "sweep": sweep, "peaks": peaks,
+        "mode_overhead_pct_all": overhead_all, "sweep": sweep, "workloads": workloads,
+        "peaks": peaks,
     }
     print(json.dumps(line))
     if world > 1:

@@ -141,6 +141,31 @@ int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
                        pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
                        pfa_stream_t stream);
 
+/* Options of pfa_attn_bwd_ex (no counterpart in the paper), OR-ed into `flags`. */
+#define PFA_BWD_DQ_DETERMINISTIC 1u /* dQ by a separate query-outer pass: one CTA sums each
+                                       dQ row over the key tiles in a fixed order into FP32,
+                                       so repeated calls give identical bits */
+#define PFA_BWD_DQ_SPLIT 2u         /* (implies the query-outer pass) dS enters the dQ product
+                                       as two BF16 terms, hi = bf16(dS) and lo = bf16(dS - hi):
+                                       about 16 significant bits instead of 8. For inputs where
+                                       keys that share a large feature get nearly cancelling dS
+                                       (a sink key copied into other positions), where the single
+                                       BF16 cast of dS dominates the error of dQ. */
+
+/* The backward pass of pfa_attn_bwd with options (no counterpart in the paper).
+ * flags == 0 is pfa_attn_bwd exactly. With PFA_BWD_DQ_DETERMINISTIC or
+ * PFA_BWD_DQ_SPLIT the key-outer kernel computes dK and dV only, and a
+ * query-outer pass recomputes S, P, dP and dS per query tile to form
+ * dQ = alpha dS K (the equation of pfa_attn_bwd, [PK] equations): it costs two
+ * more products per tile pair (S and dP again) and, with the split, a second dQ
+ * product. dq_accum is then not used and may be NULL. Other unknown flag bits
+ * return PFA_ERR_INVALID_ARG. Same arguments, layouts and checks as
+ * pfa_attn_bwd otherwise. */
+int pfa_attn_bwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                    const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                    float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                    unsigned flags, pfa_stream_t stream);
+
 /* The same backward pass for callers that cannot allocate device memory (no
  * counterpart in the paper; this is a deployment convenience). Some callers are
  * not allowed to call cudaMalloc at all: runtimes that reserve all device memory
@@ -180,7 +205,8 @@ int pfa_device_error(int clear);
 
 /* Where the first bounded wait that gave up (PFA_DEVERR_TIMEOUT) since the last
  * pfa_device_error(1) was: 0 if none, else kernel id in bits 56-59 (1 forward,
- * 2 backward, 3 delta via dP o P, 4 pfa_wait_probe), bit 55 set for a teardown
+ * 2 backward, 3 delta via dP o P, 4 pfa_wait_probe, 5 the query-outer dQ pass), bit 55
+ * set for a teardown
  * (drain) wait,
  * bit 54 the awaited phase parity, bits 32-53 the barrier's byte offset in the
  * kernel's shared memory, bits 0-31 blockIdx.x. Negative: a PFA_ERR_* code.

@@ -17,12 +17,12 @@ reference, closed forms for N = 1 and causal row 0, shift invariance across
 the three fix modes, the delta identity, central finite differences of the
 backward pass, and brute-force counts on integer-valued inputs.
 """
-from .attention import (EPS_SHIFT, attn_bwd, attn_delta, attn_delta_alt, attn_fwd,
+from .attention import (EPS_SHIFT, attn_bwd, attn_bwd_rows, attn_delta, attn_delta_alt, attn_fwd,
                         attn_fwd_head, fix_shift, scores, visible)
 from .bf16 import BF16_ONE_THRESHOLD, bf16_rne, bf16_sum, fp32, ftz32
 
 __all__ = [
-    "EPS_SHIFT", "attn_bwd", "attn_delta", "attn_delta_alt", "attn_fwd", "attn_fwd_head",
+    "EPS_SHIFT", "attn_bwd", "attn_bwd_rows", "attn_delta", "attn_delta_alt", "attn_fwd", "attn_fwd_head",
     "fix_shift", "scores", "visible", "BF16_ONE_THRESHOLD", "bf16_rne", "bf16_sum", "fp32",
     "ftz32",
 ]

@@ -70,6 +70,7 @@ __all__ = [
     "attn_delta",
     "attn_delta_alt",
     "attn_bwd",
+    "attn_bwd_rows",
 ]
 
 # The extra shift 2^-5 of mode 2 (BN "Key claims" and "Method", Algorithm 1).
@@ -292,3 +293,21 @@ def attn_bwd(q, k, v, do, lse, delta, *, causal=False, scale=None, emulate_bf16=
         dq, dk = (bf16_rne(fp32(fp32(x) * a32)).astype(np.float64) for x in (dq, dk))
         dv = bf16_rne(fp32(dv)).astype(np.float64)
     return {"dq": dq, "dk": dk, "dv": dv}
+
+
+def attn_bwd_rows(qh, kh, vh, doh, lse_rows, delta_rows, rows, *, causal=False, scale=None) -> np.ndarray:
+    """dQ of selected query rows of one head in float64 (qh, doh [R, d] the rows themselves;
+    kh, vh [N, d]; ``rows`` their indices, for the causal range): over the visible keys,
+    P_i = exp(S_i - lse_i), dP_i = dO_i V^T, dS_i = scale P_i o (dP_i - delta_i), dQ_i = dS_i K
+    (PK "수식", paper §3.3.1). The rows of :func:`attn_bwd`'s dQ, without forming the other
+    rows: long sequences are checked on sampled rows."""
+    d = qh.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.asarray(rows, dtype=np.int64)
+    s = scale * (qh @ kh.T)
+    vis = visible(rows, kh.shape[0], causal)
+    p = np.where(vis, np.exp(s - np.asarray(lse_rows, dtype=np.float64)[:, None]), 0.0)
+    dp = doh @ vh.T
+    ds = scale * p * (dp - np.asarray(delta_rows, dtype=np.float64)[:, None])
+    return ds @ kh

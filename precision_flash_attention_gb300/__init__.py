@@ -15,13 +15,14 @@ import math
 
 import torch
 
-from ._lib import (EXPORTS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_noalloc, attn_delta, attn_delta_alt,
-                   attn_fwd, bwd_workspace_bytes, device_error, device_error_site, load,
-                   status_string, wait_probe)
+from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, EXPORTS, PfaError, attn_bwd, attn_bwd_accum,
+                   attn_bwd_ex, attn_bwd_noalloc, attn_delta, attn_delta_alt, attn_fwd,
+                   bwd_workspace_bytes, device_error, device_error_site, load, status_string,
+                   wait_probe)
 
 __all__ = [
-    "EXPORTS", "PfaError", "attn_fwd", "attn_delta", "attn_delta_alt", "attn_bwd", "attn_bwd_accum",
-    "attn_bwd_noalloc",
+    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "EXPORTS", "PfaError", "attn_fwd", "attn_delta",
+    "attn_delta_alt", "attn_bwd", "attn_bwd_accum", "attn_bwd_ex", "attn_bwd_noalloc",
     "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "wait_probe",
     "forward", "backward",
     "StabilizedAttention", "new_counters",
@@ -44,12 +45,19 @@ def forward(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3
     return o, lse
 
 
-def backward(q, k, v, o, lse, do, *, causal=False, scale=None, delta_mode=0, stream=None,
-             workspace=None):
-    """delta (rowsum(dO o O), or rowsum(dP o P) with ``delta_mode=1``) then pfa_attn_bwd.
+DQ_MODES = {"atomic": 0, "deterministic": BWD_DQ_DETERMINISTIC,
+            "split": BWD_DQ_DETERMINISTIC | BWD_DQ_SPLIT}
 
-    Returns (dq, dk, dv, delta)."""
+
+def backward(q, k, v, o, lse, do, *, causal=False, scale=None, delta_mode=0, dq_mode="atomic",
+             stream=None, workspace=None):
+    """delta (rowsum(dO o O), or rowsum(dP o P) with ``delta_mode=1``) then the backward pass.
+
+    ``dq_mode``: "atomic" (pfa_attn_bwd: per-key-tile dQ sums reduce-added into an FP32
+    workspace), "deterministic" (the query-outer dQ pass) or "split" (the query-outer pass
+    with dS as a BF16 hi + lo pair). Returns (dq, dk, dv, delta)."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
+    flags = DQ_MODES[dq_mode]
     delta = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     if delta_mode == 0:
         attn_delta(o, do, delta, stream=stream)
@@ -57,6 +65,10 @@ def backward(q, k, v, o, lse, do, *, causal=False, scale=None, delta_mode=0, str
         attn_delta_alt(q, k, v, do, lse, delta, causal=causal, scale=scale, stream=stream)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     B, H, N, d = q.shape
+    if flags:
+        attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, None, causal=causal, scale=scale,
+                    flags=flags, stream=stream)
+        return dq, dk, dv, delta
     if workspace is None:
         workspace = torch.empty(bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
                                 device=q.device)

@@ -17,13 +17,16 @@ from . import build as _build
 _LIB = None
 
 PFA_OK = 0
+# pfa_attn_bwd_ex flags (include/pfa.h)
+BWD_DQ_DETERMINISTIC = 1
+BWD_DQ_SPLIT = 2
 STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED",
                 -3: "PFA_ERR_UNSUPPORTED", -4: "PFA_ERR_LAUNCH", -5: "PFA_ERR_DEVICE",
                 -6: "PFA_ERR_TOO_LARGE"}
 
 # Every entry point declared in include/pfa.h.
 EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
-           "pfa_attn_bwd_accum", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
+           "pfa_attn_bwd_accum", "pfa_attn_bwd_ex", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
            "pfa_last_error", "pfa_device_error", "pfa_device_error_site", "pfa_wait_probe")
 
 
@@ -61,6 +64,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.pfa_attn_bwd_accum.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.pfa_attn_bwd_accum.restype = i
+    lib.pfa_attn_bwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f,
+                                    ctypes.c_uint, vp]
+    lib.pfa_attn_bwd_ex.restype = i
     lib.pfa_attn_bwd_noalloc.restype = i
     lib.pfa_bwd_workspace_bytes.argtypes = [i, i, i, i]
     lib.pfa_bwd_workspace_bytes.restype = sz
@@ -216,6 +222,24 @@ def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, sca
     _check(st, "pfa_attn_bwd")
 
 
+def attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, scale: float,
+                flags: int = 0, stream=None) -> None:
+    """pfa_attn_bwd_ex: pfa_attn_bwd with options. ``flags`` 0 is attn_bwd (dq_accum the FP32
+    workspace); BWD_DQ_DETERMINISTIC and/or BWD_DQ_SPLIT compute dQ by the query-outer pass
+    (dq_accum unused, may be None)."""
+    if flags == 0:
+        attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, causal=causal, scale=scale,
+                 stream=stream)
+        return
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do"), (dq, "dq")],
+                                  extra_k=[(dk, "dk"), (dv, "dv")],
+                                  rows=[(lse, "lse"), (delta, "delta")])
+    st = load().pfa_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
+                                _ptr(dq), _ptr(dk), _ptr(dv), None, B, Hq, Hkv, N, d,
+                                int(bool(causal)), float(scale), int(flags), _stream(stream))
+    _check(st, "pfa_attn_bwd_ex")
+
+
 def attn_bwd_accum(q, k, v, do, lse, delta, dq_accum, dk, dv, *, causal: bool, scale: float,
                    stream=None) -> None:
     """pfa_attn_bwd_accum: dq_accum (FP32 [B, H_q, N, d]) += dS K; dk, dv written."""
@@ -265,6 +289,7 @@ def device_error_site() -> dict | None:
         raise PfaError(w, "pfa_device_error_site")
     if w == 0:
         return None
-    return {"kernel": {1: "forward", 2: "backward", 3: "delta_alt", 4: "wait_probe"}.get((w >> 56) & 15, "?"),
+    return {"kernel": {1: "forward", 2: "backward", 3: "delta_alt", 4: "wait_probe",
+                       5: "dq_pass"}.get((w >> 56) & 15, "?"),
             "drain": bool((w >> 55) & 1), "parity": (w >> 54) & 1,
             "barrier_offset": (w >> 32) & 0x3FFFFF, "block": w & 0xFFFFFFFF}

@@ -23,8 +23,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpfa.so")
 STAMP = os.path.join(BUILD_DIR, "stamp.txt")
 
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_delta.cu", "attn_bwd_noalloc.cu",
-           "wait_probe.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_dq.cu", "attn_delta.cu",
+           "attn_bwd_noalloc.cu", "wait_probe.cu"]
 HEADERS = [os.path.join(CSRC, "pfa_device.cuh"), os.path.join(CSRC, "pfa_internal.h"),
            os.path.join(INCLUDE, "pfa.h")]
 
@@ -51,6 +51,7 @@ def source_digest() -> str:
 # The translation unit of each kernel; its traffic record is keyed to that file,
 # the API file that builds its launch arguments and the shared headers.
 KERNEL_SOURCES = {"attn_bwd_kernel": "attn_bwd.cu", "convert_dq_kernel": "attn_bwd.cu",
+                  "attn_dq_kernel": "attn_dq.cu",
                   "attn_fwd_kernel": "attn_fwd.cu", "delta_kernel": "attn_delta.cu",
                   "delta_alt_kernel": "attn_delta.cu"}
 

@@ -298,23 +298,28 @@ struct BwdLaunch {
 
 // The argument checks shared by pfa_attn_bwd and pfa_attn_bwd_accum, and the
 // tensor maps and arguments of the kernel (dq_accum += alpha dS K; dk, dv written).
+// dq_accum may be null only when the query-outer pass computes dQ (need_accum false).
 int bwd_check(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
               const float* lse, const float* delta, const float* dq_accum, const pfa_bf16* dk,
-              const pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d, float scale) {
-  if (!q || !k || !v || !dO || !lse || !delta || !dk || !dv || !dq_accum) return PFA_ERR_INVALID_ARG;
+              const pfa_bf16* dv, int B, int H_q, int H_kv, int N, int d, float scale,
+              bool need_accum = true) {
+  if (!q || !k || !v || !dO || !lse || !delta || !dk || !dv) return PFA_ERR_INVALID_ARG;
+  if (need_accum && !dq_accum) return PFA_ERR_INVALID_ARG;
   const int rc = check_sizes(B, H_q, H_kv, N, d);
   if (rc != PFA_OK) return rc;
   if (!good_scale(scale)) return PFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) ||
-      !aligned16(delta) || !aligned16(dk) || !aligned16(dv) || !aligned16(dq_accum))
+      !aligned16(delta) || !aligned16(dk) || !aligned16(dv) || (dq_accum && !aligned16(dq_accum)))
     return PFA_ERR_MISALIGNED;
   return PFA_OK;
 }
 
+// dq_accum null: the backward kernel skips dQ (the query-outer pass computes it).
 int bwd_prepare(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
                 const float* lse, const float* delta, float* dq_accum, pfa_bf16* dk, pfa_bf16* dv,
                 int B, int H_q, int H_kv, int N, int d, int causal, float scale, BwdLaunch* L) {
-  int rc = bwd_check(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, scale);
+  int rc = bwd_check(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, scale,
+                     dq_accum != nullptr);
   if (rc != PFA_OK) return rc;
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != PFA_OK) return rc;
@@ -322,7 +327,11 @@ int bwd_prepare(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const p
   if ((rc = tile_map(&L->tk, k, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&L->tv, v, B * H_kv, N, d)) != PFA_OK) return rc;
   if ((rc = tile_map(&L->tdo, dO, B * H_q, N, d)) != PFA_OK) return rc;
-  if ((rc = f32_box_map(&L->tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
+  if (dq_accum != nullptr) {
+    if ((rc = f32_box_map(&L->tdq, dq_accum, B * H_q, N, d)) != PFA_OK) return rc;
+  } else {
+    L->tdq = CUtensorMap{};   // not used by the kernel that skips dQ
+  }
   // dK, dV leave through 64-column x 32-row boxes (d = 64: one drain warp's rows).
   if ((rc = tile_map(&L->tdk, dk, B * H_kv, N, d, 32)) != PFA_OK) return rc;
   if ((rc = tile_map(&L->tdv, dv, B * H_kv, N, d, 32)) != PFA_OK) return rc;
@@ -370,11 +379,43 @@ int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
                        const float* lse, const float* delta, float* dq_accum, pfa_bf16* dk, pfa_bf16* dv,
                        int B, int H_q, int H_kv, int N, int d, int causal, float scale,
                        pfa_stream_t stream) {
+  if (!dq_accum) return PFA_ERR_INVALID_ARG;
   BwdLaunch L;
   const int rc =
       bwd_prepare(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, causal, scale, &L);
   if (rc != PFA_OK) return rc;
   return bwd_launch(L, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pfa_attn_bwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                    const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                    float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                    unsigned flags, pfa_stream_t stream) {
+  if (flags & ~static_cast<unsigned>(PFA_BWD_DQ_DETERMINISTIC | PFA_BWD_DQ_SPLIT))
+    return PFA_ERR_INVALID_ARG;
+  if (flags == 0)
+    return pfa_attn_bwd(q, k, v, dO, lse, delta, dq, dk, dv, dq_accum, B, H_q, H_kv, N, d, causal,
+                        scale, stream);
+  // The query-outer pass computes dQ; the key-outer kernel only dK and dV.
+  if (!dq) return PFA_ERR_INVALID_ARG;
+  int rc = bwd_check(q, k, v, dO, lse, delta, nullptr, dk, dv, B, H_q, H_kv, N, d, scale, false);
+  if (rc != PFA_OK) return rc;
+  if (!aligned16(dq)) return PFA_ERR_MISALIGNED;
+  BwdLaunch L;
+  if ((rc = bwd_prepare(q, k, v, dO, lse, delta, nullptr, dk, dv, B, H_q, H_kv, N, d, causal, scale,
+                        &L)) != PFA_OK)
+    return rc;
+  pfa::DqArgs da;
+  da.s = L.a.s;
+  da.lse = lse;
+  da.delta = delta;
+  da.dq = dq;
+  da.err = L.a.err;
+  da.err_site = L.a.err_site;
+  da.split = (flags & PFA_BWD_DQ_SPLIT) ? 1 : 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((rc = bwd_launch(L, st)) != PFA_OK) return rc;
+  return launched(pfa::launch_dq(L.tq, L.tk, L.tv, L.tdo, da, st));
 }
 
 const char* pfa_status_string(int status) {

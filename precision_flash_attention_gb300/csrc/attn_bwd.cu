@@ -103,7 +103,9 @@ struct BwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <int D, bool CAUSAL>
+// DQ = false leaves dQ to the query-outer pass (attn_dq.cu): no dQ product, no dS
+// staging in shared memory and no dQ drain; dK and dV are computed as always.
+template <int D, bool CAUSAL, bool DQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc_warp(&tmQ);
         tma_prefetch_desc_warp(&tmdO);
         if (L::kTmaDQ) {
-          tma_prefetch_desc_warp(&tmdQ);
+          if (DQ) tma_prefetch_desc_warp(&tmdQ);
           tma_prefetch_desc_warp(&tmdK);
           tma_prefetch_desc_warp(&tmdV);
         }
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_warp(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl))) break;
           // With dQ over the dP^T columns (d = 128), dP^T(0) waits until the
           // previous item's last dQ has been drained.
-          if (!L::kDSDouble && g > 0 && !(ok = wait_warp(bar(L::bDQFree), (g - 1) & 1, ctl))) break;
+          if (DQ && !L::kDSDouble && g > 0 && !(ok = wait_warp(bar(L::bDQFree), (g - 1) & 1, ctl))) break;
           tc_fence_after();
           issue_s(g);
           issue_dp(g);
@@ -358,6 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) PFA_BWD_TRACE(0, 44, gg);
             // dK(i) is the last reader of this Q / dO stage (dQ reads dS and K).
             umma_commit_warp(bar(L::bQEmpty + s));
+            if constexpr (!DQ) {
+              // dP^T(i+1) overwrites dS^T(i) after dK(i) has read it (issue order).
+              if (more) issue_dp(gg + 1);
+              continue;
+            }
             if constexpr (L::kDSDouble) {
               // dP^T(i+1) overwrites dS^T(i) after dK(i) has read it; dQ(i) reads its
               // own dS buffer and waits only until dQ(i-1) has left TMEM.
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
         const Item itm = decode(item);
         QCursor qc = first_of(itm);
-        for (int i = 0; ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
+        for (int i = 0; DQ && ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
         const int it = g;
         if (!(ok = wait_warp(bar(L::bDQFull), it & 1, ctl))) break;
         if (lane == 0 && quarter == 0) PFA_BWD_TRACE(5, 13, it);
@@ -657,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(tmem + L::kColDP + lane_off + 32 * grp, pk);
         // dS^T row into the swizzled [keys][queries] buffer: panel grp / 2, 16-byte
         // chunks 4 (grp % 2) .. 4 (grp % 2) + 3 of the 128-byte row.
-        {
+        if constexpr (DQ) {
           // The last reader of this buffer, dQ(i-2) (one buffer: dQ(i-1)), was
           // issued before dP^T(i); that product's commit, which this warp waited
           // for, arrives only after every earlier product has completed.
@@ -667,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c)
             st_shared_v4(rowb + sw128_offset(r, 4 * (grp & 1) + c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
                          pk[4 * c + 3]);
+          if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 18, i);
+          fence_proxy_async_smem();
         }
-        if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 18, i);
-        fence_proxy_async_smem();
         tmem_st_wait();
         if (lane == 0 && quarter == 0 && grp < 3) PFA_BWD_TRACE(1 + grp, 10, i);
         tc_fence_before();
@@ -728,12 +735,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool DQ>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                          const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D>;
-  auto kern = attn_bwd_kernel<D, CAUSAL>;
+  auto kern = attn_bwd_kernel<D, CAUSAL, DQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   // Persistent: one CTA per SM (at most one per work item).
@@ -763,16 +770,24 @@ __global__ void convert_dq_kernel(const float4* __restrict__ src, uint2* __restr
   }
 }
 
+template <bool DQ>
+cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
+                         const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
+  if (a.s.d == 64)
+    return a.s.causal ? launch_bwd_t<64, true, DQ>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
+                      : launch_bwd_t<64, false, DQ>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
+  return a.s.causal ? launch_bwd_t<128, true, DQ>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
+                    : launch_bwd_t<128, false, DQ>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream) {
-  if (a.s.d == 64)
-    return a.s.causal ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
-                      : launch_bwd_t<64, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
-  return a.s.causal ? launch_bwd_t<128, true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
-                    : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
+  return a.dq_accum != nullptr ? dispatch_bwd<true>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream)
+                               : dispatch_bwd<false>(tq, tk, tv, tdo, tdq, tdk, tdv, a, stream);
 }
 
 // Zero the FP32 dQ workspace (n4 float4 values) as a kernel, so that it chains

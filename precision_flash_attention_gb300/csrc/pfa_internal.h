@@ -73,11 +73,22 @@ struct BwdArgs {
   AttnShape s;
   const float* lse;
   const float* delta;
-  float* dq_accum;         // fp32 [B, Hq, N, d], zeroed before the launch
+  float* dq_accum;         // fp32 [B, Hq, N, d], zeroed before the launch; null: no dQ (the
+                           // query-outer pass computes it)
   void* dk;                // bf16 [B, Hkv, N, d]
   void* dv;                // bf16 [B, Hkv, N, d]
   int* err;
   unsigned long long* err_site;
+};
+
+struct DqArgs {
+  AttnShape s;
+  const float* lse;
+  const float* delta;
+  void* dq;                // bf16 [B, Hq, N, d]
+  int* err;
+  unsigned long long* err_site;
+  int split;               // dS enters the dQ product as BF16 hi + lo
 };
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -93,6 +104,9 @@ cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
+// dQ = alpha dS K by the query-outer pass (deterministic; hi/lo dS when a.split).
+cudaError_t launch_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& tdo, const DqArgs& a, cudaStream_t stream);
 cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream);
 // Zeroes n4 float4 values of the dQ workspace on `stream` (a kernel, so that it
 // overlaps its neighbours by programmatic dependent launch).

@@ -28,8 +28,8 @@ from dataclasses import dataclass, field
 
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make", "gaussian", "integer_grid", "sink_heavy",
-           "large_logit_rows", "underflow_probe"]
+__all__ = ["Workload", "WORKLOADS", "make", "gaussian", "integer_grid", "signed_max_grid",
+           "sink_heavy", "large_logit_rows", "underflow_probe"]
 
 
 @dataclass(frozen=True)
@@ -126,6 +126,34 @@ def integer_grid(B, H_q, H_kv, N, d, *, causal=False, n_planted=8, seed=0) -> di
                 planted += 1
     return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
             "v": v.to(torch.bfloat16).contiguous(), "do": do.to(torch.bfloat16).contiguous()}
+
+
+def signed_max_grid(B, H_q, H_kv, N, d, *, sign, n_keys=2, seed=0) -> dict:
+    """Integer inputs whose row maxima are negative (``sign=-1``) or exactly zero (``sign=0``)
+    and repeated.
+
+    Q is binary ({0, 1}, feature 0 always 1 for ``sign=-1``) and K holds integers in
+    [-3, -1], so every score q.k is negative. ``n_keys`` seed-chosen keys per key/value head
+    become the row maximum for every query that sees them: the zero vector (score exactly 0)
+    for ``sign=0``, the all -1 vector (score -(number of ones of q), the largest any key in
+    [-3, -1]^d can reach) for ``sign=-1``. With a scale of 1/8 every score is an exact
+    multiple of 1/8 in FP32 and FP64, so ties are exact. V, dO ~ N(0, 1).
+    """
+    if sign not in (-1, 0):
+        raise ValueError("sign must be -1 or 0")
+    g = _gen(seed)
+    q = torch.randint(0, 2, (B, H_q, N, d), generator=g).to(torch.float32)
+    if sign < 0:
+        q[..., 0] = 1.0
+    k = torch.randint(-3, 0, (B, H_kv, N, d), generator=g).to(torch.float32)
+    for b in range(B):
+        for h in range(H_kv):
+            for j in torch.randperm(N, generator=g)[:n_keys].tolist():
+                k[b, h, j] = 0.0 if sign == 0 else -1.0
+    v = _normal((B, H_kv, N, d), 1.0, g)
+    do = _normal((B, H_q, N, d), 1.0, g)
+    return {n: t.to(torch.bfloat16).contiguous() for n, t in
+            (("q", q), ("k", k), ("v", v), ("do", do))}
 
 
 # Planted score patterns over two 128-key tiles (raw scores K / 8 for one-hot

@@ -27,7 +27,8 @@ def to_dev(t: dict) -> dict:
     return {n: x.cuda() for n, x in t.items()}
 
 
-def run_gpu(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True, delta_mode=0):
+def run_gpu(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True, delta_mode=0,
+            dq_mode="atomic"):
     """Forward (+ delta + backward) on the GPU; returns numpy float64 results and counters."""
     d = to_dev(t)
     cnt = pfa.new_counters()
@@ -36,7 +37,7 @@ def run_gpu(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True, d
     out = {"o": o, "lse": lse}
     if bwd:
         dq, dk, dv, delta = pfa.backward(d["q"], d["k"], d["v"], o, lse, d["do"], causal=causal,
-                                         scale=scale, delta_mode=delta_mode)
+                                         scale=scale, delta_mode=delta_mode, dq_mode=dq_mode)
         out.update(dq=dq, dk=dk, dv=dv, delta=delta)
     torch.cuda.synchronize()
     assert pfa.device_error(clear=True) == 0
@@ -114,3 +115,35 @@ def oracle_group_emulated(t: dict, b: int, hk: int, *, causal, scale, fix_mode, 
                          emulate_bf16=True)
     return {"o": f["o"][0], "lse": f["lse"][0], "dq": gr["dq"][0], "dk": gr["dk"][0, 0],
             "dv": gr["dv"][0, 0], "heads": hs}
+
+
+def sampled_rows(N: int, n: int = 256, seed: int = 0) -> np.ndarray:
+    """n query rows of a length-N sequence: the first and last 16 and a seeded random rest."""
+    rng = np.random.default_rng(seed)
+    edge = np.concatenate([np.arange(16), np.arange(N - 16, N)])
+    mid = rng.choice(np.arange(16, N - 16), n - len(edge), replace=False)
+    return np.sort(np.concatenate([edge, mid]))
+
+
+def check_sampled_rows(t: dict, got: dict, rows, *, causal, scale, fix_mode, beta=2.0, eps=1e-3):
+    """O, lse and dQ of the given rows of EVERY (batch, query head) against the float64 oracle
+    (forward restricted to the rows, delta = rowsum(dO o O) of those rows, dQ rows)."""
+    B, Hq = t["q"].shape[:2]
+    g = Hq // t["k"].shape[1]
+    acc = {n: ([], []) for n in ("o", "lse", "dq")}
+    for b in range(B):
+        for h in range(Hq):
+            qh, doh = f64(t["q"][b, h]), f64(t["do"][b, h])
+            kh, vh = f64(t["k"][b, h // g]), f64(t["v"][b, h // g])
+            r = oracle.attn_fwd_head(qh, kh, vh, causal=causal, scale=scale, fix_mode=fix_mode,
+                                     beta=beta, eps=eps, rows=rows)
+            delta = oracle.attn_delta(r["o"][None, None], doh[rows][None, None])[0, 0]
+            dq = oracle.attn_bwd_rows(qh[rows], kh, vh, doh[rows], r["lse"], delta, rows,
+                                      causal=causal, scale=scale)
+            for n, ref in (("o", r["o"]), ("lse", r["lse"]), ("dq", dq)):
+                acc[n][0].append(got[n][b, h, rows])
+                acc[n][1].append(ref)
+    cat = {n: (np.concatenate(a), np.concatenate(r)) for n, (a, r) in acc.items()}
+    assert_fwd_close({"o": cat["o"][0], "lse": cat["lse"][0]},
+                     {"o": cat["o"][1], "lse": cat["lse"][1]}, "sampled rows")
+    assert_bwd_close({"dq": cat["dq"][0]}, {"dq": cat["dq"][1]}, "sampled rows", names=("dq",))

@@ -145,3 +145,24 @@ def test_accumulate_and_noalloc_entry_points_validate(lib):
     if _no_device():
         bad[12] = 1024                                   # 8*16*1024*64 = 8,388,608: fits
         assert lib.pfa_attn_bwd_noalloc(*bad) != too_large
+
+
+def test_bwd_ex_validates(lib):
+    inv, mis = -1, -2
+    args = [A] * 10 + [1, 2, 1, 64, 64, 1, 0.125, 0, None]
+    bad = list(args)
+    bad[17] = 4                          # an unknown flag bit
+    assert lib.pfa_attn_bwd_ex(*bad) == inv
+    bad = list(args)
+    bad[17], bad[6] = 1, None            # the query-outer pass needs dq
+    assert lib.pfa_attn_bwd_ex(*bad) == inv
+    bad = list(args)
+    bad[17], bad[6] = 3, A + 2           # misaligned dq
+    assert lib.pfa_attn_bwd_ex(*bad) == mis
+    bad = list(args)
+    bad[9] = None                        # flags 0 is pfa_attn_bwd: the workspace is required
+    assert lib.pfa_attn_bwd_ex(*bad) == inv
+    if _no_device():
+        bad = list(args)
+        bad[17], bad[9] = 2, None        # with the query-outer pass dq_accum may be NULL
+        assert lib.pfa_attn_bwd_ex(*bad) not in (inv, mis)

@@ -128,3 +128,20 @@ def test_emulated_backward_close_to_float64():
                          causal=True, emulate_bf16=True)
     for name in ("dq", "dk", "dv"):
         assert _rel(ge[name], g[name]) < 1e-2, name
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_rows_are_rows_of_the_full_backward(causal):
+    # attn_bwd_rows is attn_bwd's dQ restricted to some rows (the sampled-row check of long
+    # sequences); attn_bwd is pinned by finite differences and autograd above.
+    t = inputs.gaussian(1, 2, 1, 70, 16, std_qkv=1.0, seed=12)
+    q, k, v, do = (_np(t[n]) for n in ("q", "k", "v", "do"))
+    f = oracle.attn_fwd(q, k, v, causal=causal, scale=0.25, fix_mode=1)
+    dl = oracle.attn_delta(f["o"], do)
+    g = oracle.attn_bwd(q, k, v, do, f["lse"], dl, causal=causal, scale=0.25)
+    rows = np.array([0, 1, 17, 33, 69])
+    for h in range(2):
+        dq = oracle.attn_bwd_rows(q[0, h, rows], k[0, 0], v[0, 0], do[0, h, rows],
+                                  f["lse"][0, h, rows], dl[0, h, rows], rows, causal=causal,
+                                  scale=0.25)
+        np.testing.assert_allclose(dq, g["dq"][0, h, rows], rtol=0, atol=1e-12)

@@ -249,3 +249,19 @@ def test_planted_tie_patterns(name):
     r = oracle.attn_fwd(q, k, v, causal=False, scale=0.125, fix_mode=1, beta=2.0, eps=0.05)
     assert r["repeated"].all() if TIE_LABELS[name] else not r["repeated"].any()
     assert r["counters"]["repeated_rows"] == (256 if TIE_LABELS[name] else 0)
+
+
+@pytest.mark.parametrize("sign", [-1, 0])
+def test_signed_max_grid_has_the_promised_maxima(sign):
+    # The generator's rows that see two planted keys have a repeated maximum of the stated
+    # sign (negative, or exactly zero); the GPU tests rely on it to reach mode 1's r_m <= 0
+    # branches.
+    from precision_flash_attention_gb300 import inputs
+    t = inputs.signed_max_grid(1, 2, 1, 200, 64, sign=sign, n_keys=3, seed=1)
+    q, k, v = (t[n].double().numpy() for n in ("q", "k", "v"))
+    f = oracle.attn_fwd(q, k, v, scale=0.125, fix_mode=0)
+    assert f["repeated"].all()
+    assert (f["m"] < 0).all() if sign < 0 else (f["m"] == 0).all()
+    f1 = oracle.attn_fwd(q, k, v, scale=0.125, fix_mode=1)
+    assert (f1["m"] == (0.0 if sign < 0 else 2.0 ** -5)).all()
+    assert f1["counters"]["ones"] == 0

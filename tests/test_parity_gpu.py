@@ -10,8 +10,9 @@ import torch
 import oracle
 import precision_flash_attention_gb300 as pfa
 from precision_flash_attention_gb300 import inputs
-from tests.gpu_helpers import (TOL_BWD_REL, assert_bwd_close, assert_fwd_close, f64, oracle_full,
-                               oracle_group, oracle_group_emulated, rel_l2, run_gpu, to_dev)
+from tests.gpu_helpers import (TOL_BWD_REL, assert_bwd_close, assert_fwd_close, check_sampled_rows,
+                               f64, oracle_full, oracle_group, oracle_group_emulated, rel_l2,
+                               run_gpu, sampled_rows, to_dev)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
 
@@ -106,6 +107,48 @@ def test_planted_tie_patterns_mixed(mode):
     assert_fwd_close(got, ref, "mixed")
 
 
+# ---------------------------------------------------------------- non-positive repeated maxima
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("sign", [-1, 0], ids=["r_m<0", "r_m=0"])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_nonpositive_repeated_maxima(mode, sign, causal, d):
+    # Mode 1's shift for a repeated maximum that is not positive: m = 0 when r_m < 0 (the
+    # priors.kr post's fix paragraph, paper §4 equation) and m = 2^-5 when r_m = 0 (a reading:
+    # the pages name only the two signed cases); mode 2 subtracts r_m + 2^-5 in both. Integer
+    # scores (multiples of 1/8) make the ties exact, so the counters must match bit for bit.
+    B, Hq, Hkv, N = 1, 2, 1, 300
+    t = inputs.signed_max_grid(B, Hq, Hkv, N, d, sign=sign, n_keys=3, seed=17 + d + sign)
+    q, k, v = (f64(t[n]) for n in ("q", "k", "v"))
+    kw = dict(causal=causal, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
+    ref = oracle.attn_fwd(q, k, v, **kw)
+    emu = oracle.attn_fwd(q, k, v, emulate_bf16=True, **kw)
+    r_m = oracle.attn_fwd(q, k, v, causal=causal, scale=0.125, fix_mode=0)["m"]
+    # Repeated rows with the intended sign of r_m (early causal rows that see no planted key
+    # can also tie, at a negative integer maximum): the branch is really taken, many times.
+    sel = ref["repeated"] & ((r_m < 0) if sign < 0 else (r_m == 0))
+    assert sel.sum() >= (100 if causal else Hq * N)
+    if mode == 1:
+        assert (ref["m"][sel] == (0.0 if sign < 0 else 2.0 ** -5)).all()
+    got = run_gpu(t, bwd=mode == 1, **kw)
+    assert got["counters"] == emu["counters"] == ref["counters"]
+    assert got["counters"]["nonfinite_rows"] == 0
+    assert_fwd_close(got, ref, f"mode {mode} sign {sign}")
+    if mode == 1:
+        # The tied keys are identical, so dQ = dS K nearly cancels along their shared direction
+        # and one BF16 rounding of dS moves it by percent: the default path's dQ is held to be
+        # no worse than the BF16-emulating oracle's (same cast points), and the query-outer pass
+        # with the hi + lo dS to the float64 tolerance. dK and dV are float64-close either way.
+        full = oracle_full(t, **kw)
+        assert_bwd_close(got, full, "signed maxima", names=("dk", "dv"))
+        e = oracle_group_emulated(t, 0, 0, **kw)
+        e_emu = rel_l2(e["dq"], full["dq"][0])
+        e_gpu = rel_l2(got["dq"][0], full["dq"][0])
+        assert e_gpu <= max(TOL_BWD_REL, 1.5 * e_emu), (e_gpu, e_emu)
+        split = run_gpu(t, dq_mode="split", **kw)
+        assert_bwd_close(split, full, "signed maxima (split dS)")
+
+
 # ---------------------------------------------------------------- ragged shapes
 RAGGED = [
     # B, Hq, Hkv, N, d, causal
@@ -151,6 +194,21 @@ def test_delta_alt_equals_delta():
     np.testing.assert_allclose(f64(d0), exact, rtol=1e-5, atol=1e-5)
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 1, 300, 128, True), (2, 2, 2, 129, 128, False),
+                                   (1, 4, 2, 640, 128, True)], ids=lambda s: "x".join(map(str, s)))
+def test_delta_alt_d128(shape):
+    # delta = rowsum(dP o P) from the d = 128 instantiation of the tcgen05 kernel, and the
+    # backward pass fed with it, against the float64 oracle.
+    B, Hq, Hkv, N, d, causal = shape
+    t = inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.5, std_do=1.0, seed=N)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(t, causal=causal, scale=scale, fix_mode=1, beta=2.0, delta_mode=1)
+    ref = oracle_full(t, causal=causal, scale=scale, fix_mode=1, beta=2.0)
+    assert rel_l2(got["delta"], ref["delta"]) <= TOL_BWD_REL
+    assert_fwd_close(got, ref, f"{shape}")
+    assert_bwd_close(got, ref, f"{shape} delta_mode 1")
+
+
 # ---------------------------------------------------------------- full-size workloads
 def test_gpt2_small_layer_all_heads():
     # B=8, H=12, N=1024, d=64, causal, modes 0 and 1 (beta=2): every head against the oracle.
@@ -188,20 +246,31 @@ def _check_groups(t, got, groups, *, causal, scale, mode, beta, dq_emulated=Fals
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_sink_heavy(mode):
-    # delta = rowsum(dP o P), the alternative the paper found stable (its §3.2): O, lse, dK
-    # and dV within the float64 tolerances. dQ is held to the BF16-emulating oracle: the
-    # BF16 cast of dS against the sink key's feature of 48 moves dQ by about 12% from float64
-    # in the oracle's own emulation (exact lse and delta), the same amount as on the GPU.
+    # delta = rowsum(dP o P), the alternative the paper found stable (its §3.2), and dQ from the
+    # query-outer pass with dS as a BF16 hi + lo pair: every output within the float64
+    # tolerances of the contract, dQ included. (A single BF16 dS moves dQ by about 12% on this
+    # input, in the oracle's own emulation as on the GPU: copies of the sink key share its
+    # feature of 48 and their dS nearly cancel along it.)
     t = inputs.make("sink", seed=0)
-    got = run_gpu(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0, delta_mode=1)
-    _check_groups(t, got, [(0, 0), (3, 11), (1, 5)], causal=True, scale=0.125, mode=mode, beta=2.0,
-                  dq_emulated=True, delta_mode=1)
+    got = run_gpu(t, causal=True, scale=0.125, fix_mode=mode, beta=2.0, delta_mode=1,
+                  dq_mode="split")
+    _check_groups(t, got, [(0, 0), (3, 11), (1, 5)], causal=True, scale=0.125, mode=mode, beta=2.0)
     c = got["counters"]
     assert c["nonfinite_rows"] == 0
     assert c["repeated_rows"] > 0.1 * 4 * 12 * 2048  # the planted duplicates
     if mode > 0:
         # the fix leaves at most the single maximum of each non-repeated row at 1.0
         assert c["ones"] <= 4 * 12 * 2048 - c["repeated_rows"] + 64
+
+
+def test_sink_heavy_single_bf16_ds_matches_emulation():
+    # The default backward (one BF16 dS operand, dQ reduce-added per key tile): O, lse, dK and
+    # dV within the float64 tolerances; dQ against the BF16-emulating oracle, which rounds dS
+    # where the kernel does.
+    t = inputs.make("sink", seed=0)
+    got = run_gpu(t, causal=True, scale=0.125, fix_mode=1, beta=2.0, delta_mode=1)
+    _check_groups(t, got, [(0, 0), (2, 7)], causal=True, scale=0.125, mode=1, beta=2.0,
+                  dq_emulated=True, delta_mode=1)
 
 
 def test_sink_heavy_delta_from_bf16_output():
@@ -229,22 +298,74 @@ def test_sink_heavy_delta_from_bf16_output():
 
 
 def test_long_context():
+    # B=2, H=16, N=8192, d=128, mode 1 with beta = 4: O, lse and dQ on 256 sampled rows of every
+    # head (the first and last 16 rows included), dK and dV of three whole key/value heads.
     t = inputs.make("long", seed=0)
     scale = 1.0 / math.sqrt(128)
     got = run_gpu(t, causal=True, scale=scale, fix_mode=1, beta=4.0)
-    _check_groups(t, got, [(1, 15)], causal=True, scale=scale, mode=1, beta=4.0)
+    check_sampled_rows(t, got, sampled_rows(8192), causal=True, scale=scale, fix_mode=1, beta=4.0)
+    _check_groups(t, got, [(1, 15), (0, 0), (0, 9)], causal=True, scale=scale, mode=1, beta=4.0)
     assert got["counters"]["nonfinite_rows"] == 0
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2])
 def test_gqa_large_logits(mode):
+    # B=1, H_q=32, H_kv=8, N=8192, d=128: sampled rows of all 32 query heads, and two whole
+    # key/value groups (four query heads each) for dK and dV.
     t = inputs.make("gqa", seed=0)
     scale = 1.0 / math.sqrt(128)
     got = run_gpu(t, causal=True, scale=scale, fix_mode=mode, beta=2.0)
-    _check_groups(t, got, [(0, 3)], causal=True, scale=scale, mode=mode, beta=2.0)
+    check_sampled_rows(t, got, sampled_rows(8192, seed=mode), causal=True, scale=scale,
+                       fix_mode=mode, beta=2.0)
+    _check_groups(t, got, [(0, 3), (0, 7)], causal=True, scale=scale, mode=mode, beta=2.0)
     assert got["counters"]["nonfinite_rows"] == 0
     if mode == 0:
         assert got["counters"]["ones"] >= 32 * 8192
+
+
+# ---------------------------------------------------------------- query-outer dQ pass
+QOUTER_SHAPES = [(1, 1, 1, 1, 64, True), (1, 2, 1, 7, 64, False), (2, 4, 2, 300, 64, True),
+                 (1, 2, 2, 257, 128, False), (1, 4, 2, 640, 128, True), (2, 3, 1, 129, 64, False)]
+
+
+@pytest.mark.parametrize("dq_mode", ["deterministic", "split"])
+@pytest.mark.parametrize("shape", QOUTER_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_query_outer_dq(shape, dq_mode):
+    # dQ from the query-outer pass (pfa_attn_bwd_ex) against the float64 oracle, dK and dV from
+    # the key-outer kernel without its dQ product; a second call gives the same bits.
+    B, Hq, Hkv, N, d, causal = shape
+    t = inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.7, std_do=1.0, seed=3 * N + d)
+    scale = 1.0 / math.sqrt(d)
+    got = run_gpu(t, causal=causal, scale=scale, fix_mode=1, beta=2.0, dq_mode=dq_mode)
+    ref = oracle_full(t, causal=causal, scale=scale, fix_mode=1, beta=2.0)
+    assert_bwd_close(got, ref, f"{shape} {dq_mode}")
+    again = run_gpu(t, causal=causal, scale=scale, fix_mode=1, beta=2.0, dq_mode=dq_mode)
+    for n in ("dq", "dk", "dv"):
+        assert np.array_equal(got[n], again[n]), n
+
+
+def test_split_dq_is_closer_to_float64_than_single_bf16():
+    # On a sink-heavy input (copies of a sink key whose large feature carries a +6 logit) the
+    # single BF16 dS leaves dQ percent away from float64; the hi + lo pair removes that rounding.
+    # delta = rowsum(dP o P) in both, so that delta from the BF16 O does not mask the effect.
+    t = inputs.sink_heavy(1, 2, 512, 64, seed=3)
+    ref = oracle_full(t, causal=True, scale=0.125, fix_mode=1)
+    single = run_gpu(t, causal=True, scale=0.125, fix_mode=1, beta=2.0, delta_mode=1)
+    split = run_gpu(t, causal=True, scale=0.125, fix_mode=1, beta=2.0, delta_mode=1, dq_mode="split")
+    e1, e2 = rel_l2(single["dq"], ref["dq"]), rel_l2(split["dq"], ref["dq"])
+    assert e1 > 2e-2 and e2 <= TOL_BWD_REL and e2 < 0.2 * e1, (e1, e2)
+
+
+def test_bwd_ex_argument_errors():
+    t = to_dev(inputs.make("tiny"))
+    o, lse = pfa.forward(t["q"], t["k"], t["v"], scale=0.125)
+    delta = torch.empty_like(lse)
+    pfa.attn_delta(o, t["do"], delta)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    with pytest.raises(pfa.PfaError, match="INVALID_ARG"):
+        pfa.attn_bwd_ex(t["q"], t["k"], t["v"], t["do"], lse, delta, dq, dk, dv, None, causal=False,
+                        scale=0.125, flags=4)
+    assert pfa.device_error() == 0
 
 
 # ---------------------------------------------------------------- degenerate cases
@@ -371,3 +492,36 @@ def test_cuda_graph_capture_matches_eager():
         assert torch.equal(a, b)
     # dQ sums reduce-adds in arrival order: equal up to FP32 rounding of that order.
     assert rel_l2(f64(dq), f64(eager[2])) < 1e-3
+
+
+def test_cuda_graph_capture_deterministic_dq_is_bit_exact():
+    # With the query-outer dQ pass every output, dQ included, replays bit for bit.
+    t = to_dev(inputs.gaussian(2, 4, 2, 384, 64, std_qkv=0.5, std_do=1.0, seed=11))
+    q, k, v, do = t["q"], t["k"], t["v"], t["do"]
+    o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        pfa.attn_fwd(q, k, v, o, lse, causal=True, scale=0.125, fix_mode=1, beta=2.0, eps=1e-3)
+        pfa.attn_delta(o, do, delta)
+        pfa.attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, None, causal=True, scale=0.125,
+                        flags=pfa.BWD_DQ_DETERMINISTIC)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (o, lse, dq, dk, dv)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for x in (o, lse, dq, dk, dv):
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    for a, b in zip(eager, (o, lse, dq, dk, dv)):
+        assert torch.equal(a, b)
