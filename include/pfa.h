@@ -102,6 +102,48 @@ int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf
                  int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
                  float beta, float eps, pfa_counters* counters, pfa_stream_t stream);
 
+/* Training-time monitor of the forward pass (no counterpart in the paper; the
+ * quantity of paper Fig. 13 -- the rows whose maximum repeats, counted by
+ * pfa_counters -- and the two views of it that a tiled kernel can report), in
+ * DEVICE memory owned by the caller. Calls ADD to it (the caller zeroes it).
+ *   operational_ones  BF16 Pbar entries equal to 1.0 that the kernel handed to the
+ *                     Pbar V product, over every 128-key tile of every row, each
+ *                     under the shift in use for that tile (the running maximum and
+ *                     the repetition flag of the keys up to that tile). Before a
+ *                     row's final maximum is seen, its earlier tiles can carry ones
+ *                     that pfa_counters.ones (final shift only) does not count.
+ *   tie_hist[b]       rows whose maximum r_m has multiplicity b + 1 (entries within
+ *                     eps of r_m), b = 0..6, and b = 7 for multiplicity >= 8. The
+ *                     kernel counts the entries within eps of its running maximum,
+ *                     restarting when the maximum rises by more than eps: exact
+ *                     whenever distinct scores near a row's maximum lie more than
+ *                     eps apart (always when scores are exact multiples of a grid
+ *                     coarser than eps), an upper bound otherwise. */
+#define PFA_TIE_BINS 8
+typedef struct pfa_monitor {
+  int64_t operational_ones;
+  int64_t tie_hist[PFA_TIE_BINS];
+} pfa_monitor;
+
+/* Options of pfa_attn_fwd_ex (no counterpart in the paper), OR-ed into `flags`. */
+#define PFA_FWD_UNFUSED_BF16_PV 1u /* study profile, d = 64 only: each 128-key tile's
+                                      product Pbar V is rounded to BF16 and accumulated
+                                      across tiles in BF16 (Obar = bf16(bf16(Obar x corr)
+                                      + bf16(Pbar V))), and l sums the BF16 Pbar; the way an
+                                      implementation that stores the unnormalised product
+                                      in BF16 computes O ([PK] caveats: the analysed code
+                                      keeps P V in BF16). Not a fast path. */
+
+/* pfa_attn_fwd with the monitor and options (no counterpart in the paper).
+ * counters and monitor are optional (NULL); flags 0 and monitor NULL is
+ * pfa_attn_fwd exactly. PFA_FWD_UNFUSED_BF16_PV with d != 64 returns
+ * PFA_ERR_UNSUPPORTED; unknown flag bits PFA_ERR_INVALID_ARG. eps must be finite
+ * and >= 0 when a monitor is given. */
+int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
+                    int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
+                    float beta, float eps, pfa_counters* counters, pfa_monitor* monitor,
+                    unsigned flags, pfa_stream_t stream);
+
 /* delta = rowsum(dO o O) in FP32 from the BF16 forward output ([PK] three-line
  * summary and method, paper §3.2; [BN] Key claims).
  *   o, dO [B,H_q,N,d] (in); delta [B,H_q,N] (out). */

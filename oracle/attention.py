@@ -71,7 +71,13 @@ __all__ = [
     "attn_delta_alt",
     "attn_bwd",
     "attn_bwd_rows",
+    "attn_fwd_monitor",
+    "attn_fwd_unfused",
+    "TIE_BINS",
 ]
+
+# Bins of the tie-multiplicity histogram: multiplicity 1..7, and 8 or more.
+TIE_BINS = 8
 
 # The extra shift 2^-5 of mode 2 (BN "Key claims" and "Method", Algorithm 1).
 EPS_SHIFT = 2.0 ** -5
@@ -311,3 +317,109 @@ def attn_bwd_rows(qh, kh, vh, doh, lse_rows, delta_rows, rows, *, causal=False, 
     dp = doh @ vh.T
     ds = scale * p * (dp - np.asarray(delta_rows, dtype=np.float64)[:, None])
     return ds @ kh
+
+
+def attn_fwd_monitor(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3,
+                     tile=128, emulate_bf16=True) -> dict:
+    """The training-time monitor of a tiled forward pass (the repeated maxima that PK "결과"
+    (paper App. E.1, Fig. 13) tracks, and two views of them):
+
+    * ``operational_ones``: over every row and every ``tile``-key block of its visible keys,
+      in order, the entries whose BF16 Pbar equals 1.0 under the shift in use for that block:
+      the shift rule (:func:`fix_shift`) applied to the row's maximum over the keys up to the
+      block's end, with the repetition flag of those same keys (at least two of them within
+      ``eps`` of that maximum). These are the exact ones a tiled kernel hands to the Pbar V
+      product; rows whose maximum rises later can carry ones that the final shift no longer
+      has.
+    * ``tie_hist``: rows by the multiplicity of their maximum, #{j : S_ij >= r_m - eps}, in
+      bins 1..7 and >= 8 (index multiplicity - 1, capped at 7).
+
+    Scores, exponentials and the BF16 cast as in :func:`attn_fwd_head` (``emulate_bf16``
+    selects FP32 scores and an FP32 exponential)."""
+    B, Hq, Hkv, N, d = _check_shapes(q, k, v)
+    group = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    ones = 0
+    hist = np.zeros(TIE_BINS, dtype=np.int64)
+    rows = np.arange(N)
+    vis = visible(rows, N, causal)
+    for b in range(B):
+        for h in range(Hq):
+            s = np.where(vis, scores(q[b, h], k[b, h // group], scale, emulate_bf16), -np.inf)
+            r_m = s.max(axis=1)
+            mult = (s >= (r_m - eps)[:, None]).sum(axis=1)
+            hist += np.bincount(np.minimum(mult, TIE_BINS) - 1, minlength=TIE_BINS)
+            for j0 in range(0, N, tile):
+                seen = s[:, : j0 + tile]
+                m1 = seen.max(axis=1)
+                live = np.isfinite(m1)
+                rep = (seen >= (m1 - eps)[:, None]).sum(axis=1) >= 2
+                m = fix_shift(np.where(live, m1, 0.0), rep, fix_mode, beta, emulate_bf16)
+                x = s[:, j0: j0 + tile] - m[:, None]
+                if emulate_bf16:
+                    pbar = ftz32(np.exp(fp32(x)))
+                else:
+                    pbar = fp32(np.exp(x))
+                ones += int(((bf16_rne(pbar) == 1.0) & live[:, None]).sum())
+    return {"operational_ones": ones, "tie_hist": hist}
+
+
+def attn_fwd_unfused(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3,
+                     block=512) -> dict:
+    """The forward pass as an implementation that stores the unnormalised product Pbar V in
+    BF16 computes it: the paper's analysed code, FlashAttention 2 written as PyTorch
+    operations with blocks of 512 keys (PK "의심해볼 점"; the bias mechanism of PK
+    "핵심 아이디어", paper §3.3.2, and BN "Results", Fig. 6).
+
+    Per row, per ``block`` of keys in order: the running maximum and the repetition flag of
+    the keys so far give the shift m_b (:func:`fix_shift`); Pbar = BF16(exp(S - m_b)) from an
+    FP32 exponential (flushed to zero below the normal range); the block's product
+    U_b = BF16(sum_j Pbar_j V_j) is formed exactly and rounded once (an FP32-accumulating
+    BF16 matrix product with a BF16 result, the accumulation model of the pages' worked
+    traces, :func:`oracle.bf16.bf16_sum`); the accumulator follows
+    Obar = BF16(BF16(Obar * c_b) + U_b) with c_b = exp(m_(b-1) - m_b) in FP32; l = FP32
+    (l * c_b + sum of the BF16 Pbar) -- the normaliser sums the weights the product used (a
+    reading: the pages name only P V as stored in BF16). Finally O = BF16(Obar / l) and
+    lse = m + ln l (FP32). Scores are FP32 (one rounding of the exact dot, times FP32 alpha).
+
+    Returns ``o``, ``lse`` [B,H_q,N,d] / [B,H_q,N] and ``obar`` (the BF16 accumulator before
+    normalisation)."""
+    B, Hq, Hkv, N, d = _check_shapes(q, k, v)
+    group = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    rows = np.arange(N)
+    vis = visible(rows, N, causal)
+    o = np.zeros(q.shape)
+    obar_all = np.zeros(q.shape)
+    lse = np.zeros((B, Hq, N))
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // group
+            s = np.where(vis, scores(q[b, h], k[b, kv], scale, True), -np.inf)
+            m_prev = np.full(N, -np.inf)
+            l = np.zeros(N)
+            obar = np.zeros((N, d))
+            for j0 in range(0, N, block):
+                seen = s[:, : j0 + block]
+                m1 = seen.max(axis=1)
+                live = np.isfinite(m1)
+                rep = (seen >= (m1 - eps)[:, None]).sum(axis=1) >= 2
+                m = np.where(live, fix_shift(np.where(live, m1, 0.0), rep, fix_mode, beta, True),
+                             -np.inf)
+                with np.errstate(invalid="ignore"):
+                    c = np.where(np.isfinite(m_prev), ftz32(np.exp(fp32(m_prev - m))), 0.0)
+                with np.errstate(invalid="ignore"):
+                    x = np.where(live[:, None], s[:, j0: j0 + block] - m[:, None], -np.inf)
+                pbar = ftz32(bf16_rne(ftz32(np.exp(fp32(x)))))
+                l = fp32(l.astype(np.float64) * c + pbar.astype(np.float64).sum(axis=1))
+                u = bf16_rne(fp32(pbar.astype(np.float64) @ v[b, kv, j0: j0 + block]))
+                scaled = bf16_rne(fp32(obar.astype(np.float64) * c[:, None]))
+                obar = bf16_rne(fp32(scaled.astype(np.float64) + u.astype(np.float64)))
+                m_prev = m
+            with np.errstate(divide="ignore", invalid="ignore"):
+                o[b, h] = bf16_rne(fp32(obar.astype(np.float64) / l.astype(np.float64)[:, None]))
+                lse[b, h] = fp32(fp32(m_prev) + fp32(np.log(l.astype(np.float64))))
+            obar_all[b, h] = obar
+    return {"o": o, "lse": lse, "obar": obar_all}

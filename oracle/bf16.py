@@ -26,7 +26,8 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["fp32", "bf16_rne", "ftz32", "bf16_sum", "BF16_ONE_THRESHOLD"]
+__all__ = ["fp32", "bf16_rne", "ftz32", "bf16_sum", "BF16_ONE_THRESHOLD", "e4m3_rne", "e2m1_rne",
+           "mx_e2m1", "E4M3_MAX", "E2M1_MAX", "MX_BLOCK"]
 
 # Smallest FP32 value x with bf16_rne(x) == 1.0: the midpoint between 1 - 2^-8
 # (the largest BF16 value below 1) and 1.0. A tie there rounds to 1.0 because
@@ -78,3 +79,60 @@ def bf16_sum(terms) -> np.float32:
     for t in terms:
         s = np.float32(s + np.float32(t))
     return np.float32(bf16_rne(s).reshape(()))
+
+
+# --------------------------------------------------------------------------------------
+# Narrower formats, for the question PK "열린 질문" leaves open: what the bias looks like
+# when fewer mantissa bits carry the summed values (FP8, MXFP4).
+# --------------------------------------------------------------------------------------
+E4M3_MAX = 448.0   # largest finite FP8 E4M3 value: 1.75 x 2^8
+E2M1_MAX = 6.0     # largest FP4 E2M1 value: 1.5 x 2^2
+MX_BLOCK = 32      # elements sharing one scale in the MX formats
+
+
+def _round_grid(a, exp_min, mbits):
+    """Round non-negative float64 ``a`` to a binary grid with ``mbits`` stored mantissa bits
+    and smallest exponent ``exp_min`` (subnormals below 2^exp_min), nearest, ties to even."""
+    a = np.asarray(a, dtype=np.float64)
+    out = np.zeros_like(a)
+    nz = a > 0
+    e = np.floor(np.log2(np.where(nz, a, 1.0)))
+    e = np.maximum(e, exp_min)
+    ulp = np.exp2(e - mbits)
+    q = a / ulp
+    r = np.round(q)             # numpy rounds halves to even
+    out = np.where(nz, r * ulp, 0.0)
+    return out
+
+
+def e4m3_rne(x) -> np.ndarray:
+    """Round to FP8 E4M3 (4 exponent bits with bias 7, 3 stored mantissa bits, no
+    infinities): nearest, ties to even; magnitudes beyond the largest finite value 448
+    saturate to it; subnormals are 2^-9 apart below 2^-6. Returns float64 values."""
+    x = np.asarray(x, dtype=np.float64)
+    y = np.minimum(_round_grid(np.abs(x), -6, 3), E4M3_MAX)
+    return np.where(np.isnan(x), np.nan, np.copysign(y, x))
+
+
+def e2m1_rne(x) -> np.ndarray:
+    """Round to FP4 E2M1 (2 exponent bits with bias 1, 1 stored mantissa bit): the values
+    0, 0.5, 1, 1.5, 2, 3, 4, 6; nearest, ties to even; saturating at 6."""
+    x = np.asarray(x, dtype=np.float64)
+    y = np.minimum(_round_grid(np.abs(x), 0, 1), E2M1_MAX)
+    return np.copysign(y, x)
+
+
+def mx_e2m1(x, axis=-1) -> np.ndarray:
+    """MXFP4: blocks of 32 consecutive elements along ``axis`` share a power-of-two scale
+    X = 2^(floor(log2(amax)) - 2) (2 = the largest exponent of E2M1), and each element
+    becomes X * E2M1(v / X) (saturating). A block of zeros stays zero. Returns float64."""
+    x = np.moveaxis(np.asarray(x, dtype=np.float64), axis, -1)
+    n = x.shape[-1]
+    pad = (-n) % MX_BLOCK
+    xp = np.concatenate([x, np.zeros(x.shape[:-1] + (pad,))], axis=-1)
+    blocks = xp.reshape(x.shape[:-1] + (-1, MX_BLOCK))
+    amax = np.abs(blocks).max(axis=-1, keepdims=True)
+    scale = np.where(amax > 0, np.exp2(np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 2), 1.0)
+    q = e2m1_rne(blocks / scale) * scale
+    out = q.reshape(xp.shape)[..., :n]
+    return np.moveaxis(out, -1, axis)

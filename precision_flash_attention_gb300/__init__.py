@@ -15,17 +15,18 @@ import math
 
 import torch
 
-from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, EXPORTS, PfaError, attn_bwd, attn_bwd_accum,
-                   attn_bwd_ex, attn_bwd_noalloc, attn_delta, attn_delta_alt, attn_fwd,
-                   bwd_workspace_bytes, device_error, device_error_site, load, status_string,
-                   wait_probe)
+from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, EXPORTS, FWD_UNFUSED_BF16_PV, MONITOR_WORDS,
+                   TIE_BINS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_ex, attn_bwd_noalloc,
+                   attn_delta, attn_delta_alt, attn_fwd, attn_fwd_ex, bwd_workspace_bytes,
+                   device_error, device_error_site, load, status_string, wait_probe)
 
 __all__ = [
-    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "EXPORTS", "PfaError", "attn_fwd", "attn_delta",
+    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "EXPORTS", "FWD_UNFUSED_BF16_PV", "MONITOR_WORDS",
+    "TIE_BINS", "PfaError", "attn_fwd", "attn_fwd_ex", "attn_delta",
     "attn_delta_alt", "attn_bwd", "attn_bwd_accum", "attn_bwd_ex", "attn_bwd_noalloc",
     "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "wait_probe",
     "forward", "backward",
-    "StabilizedAttention", "new_counters",
+    "StabilizedAttention", "new_counters", "new_monitor",
 ]
 
 
@@ -34,14 +35,26 @@ def new_counters(device="cuda") -> torch.Tensor:
     return torch.zeros(3, dtype=torch.int64, device=device)
 
 
+def new_monitor(device="cuda") -> torch.Tensor:
+    """A zeroed int64[9] device buffer for the forward monitor: operational ones, then the
+    tie-multiplicity histogram (multiplicity 1..7, >= 8)."""
+    return torch.zeros(MONITOR_WORDS, dtype=torch.int64, device=device)
+
+
 def forward(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3, counters=None,
-            stream=None):
-    """Allocate O and lse and run pfa_attn_fwd. Returns (o, lse)."""
+            monitor=None, unfused_bf16_pv=False, stream=None):
+    """Allocate O and lse and run the forward pass (pfa_attn_fwd, or pfa_attn_fwd_ex with a
+    monitor or the unfused BF16 study profile). Returns (o, lse)."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps,
-             counters=counters, stream=stream)
+    if monitor is None and not unfused_bf16_pv:
+        attn_fwd(q, k, v, o, lse, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps,
+                 counters=counters, stream=stream)
+    else:
+        attn_fwd_ex(q, k, v, o, lse, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta,
+                    eps=eps, counters=counters, monitor=monitor,
+                    flags=FWD_UNFUSED_BF16_PV if unfused_bf16_pv else 0, stream=stream)
     return o, lse
 
 

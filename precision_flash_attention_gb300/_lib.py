@@ -17,6 +17,10 @@ from . import build as _build
 _LIB = None
 
 PFA_OK = 0
+# pfa_attn_fwd_ex flags and the monitor's size (include/pfa.h)
+FWD_UNFUSED_BF16_PV = 1
+TIE_BINS = 8
+MONITOR_WORDS = 1 + TIE_BINS
 # pfa_attn_bwd_ex flags (include/pfa.h)
 BWD_DQ_DETERMINISTIC = 1
 BWD_DQ_SPLIT = 2
@@ -25,7 +29,7 @@ STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED"
                 -6: "PFA_ERR_TOO_LARGE"}
 
 # Every entry point declared in include/pfa.h.
-EXPORTS = ("pfa_attn_fwd", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
+EXPORTS = ("pfa_attn_fwd", "pfa_attn_fwd_ex", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
            "pfa_attn_bwd_accum", "pfa_attn_bwd_ex", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
            "pfa_last_error", "pfa_device_error", "pfa_device_error_site", "pfa_wait_probe")
 
@@ -55,6 +59,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.pfa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, f, f, vp, vp]
     lib.pfa_attn_fwd.restype = i
+    lib.pfa_attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, f, f, vp, vp,
+                                    ctypes.c_uint, vp]
+    lib.pfa_attn_fwd_ex.restype = i
     lib.pfa_attn_delta.argtypes = [vp, vp, vp, i, i, i, i, vp]
     lib.pfa_attn_delta.restype = i
     lib.pfa_attn_delta_alt.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
@@ -176,6 +183,27 @@ def attn_fwd(q, k, v, o, lse, *, causal: bool, scale: float, fix_mode: int = 0,
                              float(eps), _ptr(counters) if counters is not None else None,
                              _stream(stream))
     _check(st, "pfa_attn_fwd")
+
+
+def attn_fwd_ex(q, k, v, o, lse, *, causal: bool, scale: float, fix_mode: int = 0,
+                beta: float = 2.0, eps: float = 1e-3, counters=None, monitor=None, flags: int = 0,
+                stream=None) -> None:
+    """pfa_attn_fwd_ex: pfa_attn_fwd with the monitor (int64[9]: operational ones, then the
+    8-bin tie-multiplicity histogram) and options (FWD_UNFUSED_BF16_PV)."""
+    also = []
+    for t, n, words in ((counters, "counters", 3), (monitor, "monitor", MONITOR_WORDS)):
+        if t is not None:
+            _layout(t, n, torch.int64, 1)
+            if t.numel() != words:
+                raise ValueError(f"{n} must hold {words} int64 values")
+            also.append((t, n))
+    B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(o, "o")], rows=[(lse, "lse")], also=also)
+    st = load().pfa_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, N, d,
+                                int(bool(causal)), float(scale), int(fix_mode), float(beta),
+                                float(eps), _ptr(counters) if counters is not None else None,
+                                _ptr(monitor) if monitor is not None else None, int(flags),
+                                _stream(stream))
+    _check(st, "pfa_attn_fwd_ex")
 
 
 def attn_delta(o, do, delta, *, stream=None) -> None:

@@ -212,15 +212,27 @@ extern "C" {
 int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
                  int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
                  float beta, float eps, pfa_counters* counters, pfa_stream_t stream) {
+  return pfa_attn_fwd_ex(q, k, v, o, lse, B, H_q, H_kv, N, d, causal, scale, fix_mode, beta, eps,
+                         counters, nullptr, 0u, stream);
+}
+
+int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
+                    int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
+                    float beta, float eps, pfa_counters* counters, pfa_monitor* monitor,
+                    unsigned flags, pfa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return PFA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H_q, H_kv, N, d);
   if (rc != PFA_OK) return rc;
+  if (flags & ~static_cast<unsigned>(PFA_FWD_UNFUSED_BF16_PV)) return PFA_ERR_INVALID_ARG;
+  const bool profile = (flags & PFA_FWD_UNFUSED_BF16_PV) != 0;
+  if (profile && d != 64) return PFA_ERR_UNSUPPORTED;
   if (!good_scale(scale) || fix_mode < 0 || fix_mode > 2) return PFA_ERR_INVALID_ARG;
   if (fix_mode == 1 && !(std::isfinite(beta) && beta > 1.f)) return PFA_ERR_INVALID_ARG;
-  const bool ties = fix_mode != 0 || counters != nullptr;
+  const bool ties = fix_mode != 0 || counters != nullptr || monitor != nullptr;
   if (ties && !(std::isfinite(eps) && eps >= 0.f)) return PFA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      (counters && (reinterpret_cast<uintptr_t>(counters) & 7u)))
+      (counters && (reinterpret_cast<uintptr_t>(counters) & 7u)) ||
+      (monitor && (reinterpret_cast<uintptr_t>(monitor) & 7u)))
     return PFA_ERR_MISALIGNED;
   DeviceState* dev = nullptr;
   if ((rc = current_device(&dev)) != PFA_OK) return rc;
@@ -233,13 +245,17 @@ int pfa_attn_fwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf
   a.o = o;
   a.lse = lse;
   a.counters = reinterpret_cast<long long*>(counters);
+  a.monitor = reinterpret_cast<long long*>(monitor);
   a.err = dev->err;
   a.err_site = dev->site;
   a.fix_mode = fix_mode;
   a.beta = fix_mode == 1 ? beta : 2.f;
   a.eps_raw = ties ? eps / scale : 0.f;
   a.tau_raw = static_cast<float>(kRoundToOneWindow / scale);
-  return launched(pfa::launch_fwd(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+  a.profile = profile ? 1 : 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (profile || monitor) return launched(pfa::launch_fwd_study(tq, tk, tv, a, st));
+  return launched(pfa::launch_fwd(tq, tk, tv, a, st));
 }
 
 int pfa_attn_delta(const pfa_bf16* o, const pfa_bf16* dO, float* delta, int B, int H_q, int N,

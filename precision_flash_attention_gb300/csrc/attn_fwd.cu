@@ -1,668 +1,20 @@
-// Forward kernel: S = alpha Q K^T on tcgen05 (FP32 in TMEM), the online safe
-// softmax with the repeated-maximum tracker and the per-call shift rule,
-// Pbar = exp(S - m) in FP32 cast to BF16, Obar += Pbar V on tcgen05 (FP32 in
-// TMEM), then O = Obar / l (BF16) and lse = m + ln l (FP32), plus the
-// diagnostic counters.
-//
-// The method is the one analysed in Qiu & Yao, "Why Low-Precision Transformer
-// Training Fails: An Analysis on Flash Attention" (ICLR 2026), as summarised by
-// the priors.kr post "BF16 플래시 어텐션은 왜 수천 스텝 뒤에 무너질까" (core idea,
-// equations, and the fix of paper §4) and the bud-325 note of the same title
-// (Key claims, Method / Algorithm 1).
-//
-// A work item is two adjacent 128-row Q tiles (t = 0, 1) of one (batch, query
-// head). Persistent: one CTA per SM takes items heaviest causal pairs first,
-// dealt in serpentine rounds of gridDim.x; barrier phases count across items, so setup and
-// teardown happen once per SM and the next item's Q (double buffered for
-// d = 64) and K / V stream in while the current item finishes. 384 threads,
-// one warpgroup per role group (registers are granted per warpgroup):
-//   warp 0      K / V producer (one ring of stages across items)
-//   warp 1      TMEM owner and tcgen05.mma issuer
-//   warp 2      Q producer (one pair per item)
-//   warp 3      idle
-//   warps 4..7  softmax of tile 0, warps 8..11 softmax of tile 1; one query row
-//               per thread (TMEM lane quarter = warp % 4)
-// TMEM (512 columns): S_t in [128 t, 128 t + 128), O_t in [256 + d t, 256 + d t + d).
-// Pbar_t (BF16) is the TMEM A operand of Obar_t += Pbar_t V. At d = 64 it has
-// its own columns [384 + 64 t, 448 + 64 t): once the softmax has read S_t(j)
-// into registers the tensor core computes S_t(j+1), so each softmax warpgroup
-// finds its next scores ready when it finishes a tile; the tensor core runs
-// S0_j, S1_j, PV0_{j-1}, PV1_{j-1}, ... At d = 128 (no columns left) Pbar_t is
-// written over the first 64 columns of S_t and the tensor core runs S0_j,
-// PV1_{j-1}, S1_j, PV0_j, ... so that each tile's softmax overlaps the other
-// tile's two products.
-#include "pfa_device.cuh"
-#include "pfa_trace.cuh"
-
-PFA_TRACE_BUFFER(g_pfa_fwd_trace);
-#define PFA_FWD_TRACE(slot, ev, j) PFA_TRACE_EVENT(g_pfa_fwd_trace, slot, ev, j)
+// The fused forward path: the attention forward kernel (attn_fwd.cuh) with the
+// FP32 Obar accumulator, instantiated for d = 64 and 128, the three shift modes,
+// causal or not, with or without the diagnostic counters.
+#include "attn_fwd.cuh"
 
 namespace pfa {
 namespace {
-
-constexpr int kThreads = 384;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kEpsShift = 0.03125f;  // 2^-5
-
-template <int D>
-struct FwdLayout {
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q pairs in flight
-  // d = 64: Pbar_t gets its own TMEM columns [384 + 64 t, 448 + 64 t), so the
-  // next S_t can be computed as soon as the softmax holds the current one in
-  // registers. d = 128 has no columns left and writes Pbar_t over S_t.
-  static constexpr bool kSplitP = (D == 64);
-  static constexpr uint32_t kColP = 384;
-  static constexpr int kTileBytes = kTile * D * 2;   // 128 rows x D bf16
-  static constexpr int kPanelBytes = kTile * 128;    // 128 rows x 64 bf16
-  static constexpr int kQ = 0;                       // + (buffer * 2 + t) * tile
-  static constexpr int kK = kQBufs * 2 * kTileBytes; // + stage * tile
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBars = kV + kStages * kTileBytes;
-  static constexpr int bQFull = 0;                    // + Q buffer
-  static constexpr int bQEmpty = bQFull + kQBufs;     // + Q buffer: the item's products are done
-  static constexpr int bKVFull = bQEmpty + kQBufs;    // + stage
-  static constexpr int bKVEmpty = bKVFull + kStages;  // + stage
-  static constexpr int bSFull = bKVEmpty + kStages;   // + tile
-  static constexpr int bPFull = bSFull + 2;           // + tile
-  static constexpr int bODone = bPFull + 2;           // + tile
-  static constexpr int bSFree = bODone + 2;           // + tile: the softmax holds S_t (split Pbar)
-  static constexpr int bPVDone = bSFree + 2;          // + tile: Obar_t += Pbar_t V done (split Pbar)
-  static constexpr int bDrain = bPVDone + 2;
-  static constexpr int bRegs = bDrain + 1;          // the softmax warps hold their registers
-  static constexpr int kNumBars = bRegs + 1;
-  static constexpr int kTmemSlot = kBars + kNumBars * 8;
-  static constexpr int kAbort = kTmemSlot + 4;
-  static constexpr int kBytes = kAbort + 4;
-  static_assert(kBytes <= 232448, "shared memory budget");
-};
-
-template <int D, int MODE, bool CAUSAL, bool COUNT>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using L = FwdLayout<D>;
-  // The tie tracker (running top-2) is needed by the fix modes and by the
-  // repeated-row counter, which is reported in every mode.
-  constexpr bool kTies = MODE > 0 || COUNT;
-  extern __shared__ __align__(1024) uint8_t smem[];
-  const uint32_t sbase = smem_u32(smem);
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  PFA_TRACE_DECL();
-
-  const AttnShape& sh = args.s;
-  const int N = sh.N;
-  const int n_kt = (N + kTile - 1) / kTile;   // key tiles == query tiles
-  const int n_pairs = (n_kt + 1) / 2;
-  const int BHq = sh.B * sh.Hq;
-  const int n_items = n_pairs * BHq;
-  const int item0 = static_cast<int>(blockIdx.x);
-  const int stride = static_cast<int>(gridDim.x);
-  // The k-th item of this CTA: rounds of gridDim.x items, taken left to right in
-  // even rounds and right to left in odd ones, so that a CTA given a heavy item
-  // early gets a light one in the next round.
-  auto item_at = [&](int k) { return k * stride + ((k & 1) ? stride - 1 - item0 : item0); };
-  // Work item -> (pair of query tiles, batch and query head); pairs heaviest first.
-  struct Item {
-    int bh, bh_kv, qt0, last0, last1, n_iter;
-    bool has1;
-  };
-  auto decode = [&](int item) {
-    Item it;
-    it.bh = item % BHq;
-    const int pair = n_pairs - 1 - item / BHq;
-    const int b = it.bh / sh.Hq, h = it.bh % sh.Hq;
-    it.bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
-    it.qt0 = 2 * pair;
-    it.has1 = it.qt0 + 1 < n_kt;
-    // Last key tile each query tile visits (-1: the tile does not exist).
-    it.last0 = CAUSAL ? it.qt0 : n_kt - 1;
-    it.last1 = it.has1 ? (CAUSAL ? it.qt0 + 1 : n_kt - 1) : -1;
-    it.n_iter = max(it.last0, it.last1) + 1;
-    return it;
-  };
-
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
-  auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
-  const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 1u};
-
-  if (threadIdx.x == 0) {
-    *abort_flag = (sbase & 1023u) ? 1 : 0;
-    if (sbase & 1023u) atomicOr(args.err, PFA_DEVERR_SMEM_ALIGN);
-    for (int qb = 0; qb < L::kQBufs; ++qb) {
-      mbar_init(bar(L::bQFull + qb), 1);
-      mbar_init(bar(L::bQEmpty + qb), 1);
-    }
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::bKVFull + s), 1);
-      mbar_init(bar(L::bKVEmpty + s), 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(L::bSFull + t), 1);
-      mbar_init(bar(L::bPFull + t), 4);
-      mbar_init(bar(L::bODone + t), 1);
-      mbar_init(bar(L::bSFree + t), 4);
-      mbar_init(bar(L::bPVDone + t), 1);
-    }
-    mbar_init(bar(L::bDrain), 1);
-    mbar_init(bar(L::bRegs), 8);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // Setup done: let the next kernel on the stream be scheduled as CTAs leave, and
-  // order every global access after the kernel before this one.
-  grid_launch_dependents();
-  grid_dependency_wait();
-  // Register split per warpgroup. The block is launched with 168 registers per
-  // thread (384 x 168 = 64512). Warpgroup 0 (producers, MMA, one idle warp)
-  // drops to 64 and the two softmax warpgroups rise to 216: 128 x 64 + 256 x 216
-  // = 63488. Each group returns to 168 before the common teardown.
-  if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
-    if (*abort_flag == 0) {
-    if (warp == 0) {
-      // ---------------- K / V producer (whole warp, one elected lane issues) ----------------
-      // One ring of stages for the key tiles of all items of this CTA.
-      tma_prefetch_desc_warp(&tmK);
-      tma_prefetch_desc_warp(&tmV);
-      int gk = 0;   // key tiles issued
-      bool ok = true;
-      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
-        const Item it = decode(item);
-        for (int j = 0; j < it.n_iter; ++j, ++gk) {
-          const int s = gk % L::kStages;
-          if (!(ok = wait_warp(bar(L::bKVEmpty + s), ((gk / L::kStages) & 1) ^ 1, ctl))) break;
-          mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
-            tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
-          }
-        }
-      }
-      // Drain: every issued copy has landed before shared memory is released.
-      for (int j = gk > L::kStages ? gk - L::kStages : 0; j < gk; ++j)
-        wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
-    } else if (warp == 2) {
-      // ---------------- Q producer: the pair of query tiles of each item ----------------
-      tma_prefetch_desc_warp(&tmQ);
-      int ti = 0;   // items issued
-      bool ok = true;
-      for (int k = 0, item = item0; item < n_items; ++k, item = item_at(k), ++ti) {
-        const Item it = decode(item);
-        const int qb = ti % L::kQBufs;
-        if (!(ok = wait_warp(bar(L::bQEmpty + qb), ((ti / L::kQBufs) & 1) ^ 1, ctl))) break;
-        mbar_arrive_expect_tx_warp(bar(L::bQFull + qb), (it.has1 ? 2 : 1) * L::kTileBytes);
-        for (int t = 0; t < (it.has1 ? 2 : 1); ++t)
-          for (int p = 0; p < D / 64; ++p)
-            tma_load_3d_warp(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                             bar(L::bQFull + qb), p * 64, (it.qt0 + t) * kTile, it.bh);
-        // With one Q buffer the next pair waits for this item: start it into L2.
-        if (L::kQBufs == 1 && item_at(k + 1) < n_items) {
-          const Item nx = decode(item_at(k + 1));
-          for (int t = 0; t < (nx.has1 ? 2 : 1); ++t)
-            for (int p = 0; p < D / 64; ++p) tma_prefetch_l2_3d_warp(&tmQ, p * 64, (nx.qt0 + t) * kTile, nx.bh);
-        }
-      }
-      for (int i = ti > L::kQBufs ? ti - L::kQBufs : 0; i < ti; ++i)
-        wait_drain(bar(L::bQFull + i % L::kQBufs), (i / L::kQBufs) & 1, ctl);
-      (void)ok;
-    } else if (warp == 1) {
-      // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
-      // S_t = Q_t K_j^T from Q buffer qb and K/V stage s.
-      auto issue_s = [&](int t, int qb, int s) {
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          umma_bf16_warp(tmem + 128 * t,
-                         sdesc_sw128(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + koff, 16, 1024),
-                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
-        }
-        umma_commit_warp(bar(L::bSFull + t));
-      };
-      // Obar_t (+)= Pbar_t V_j; Pbar_t is 64 BF16-pair columns (its own with the
-      // split layout, else the first 64 of S_t), 8 columns per K step.
-      auto issue_pv = [&](int t, int s, int j) {
-        const uint32_t tp = tmem + (L::kSplitP ? L::kColP + 64u * t : 128u * t);
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_tmem_a_warp(tmem + 256 + D * t, tp + 8 * kk,
-                                sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
-                                            L::kPanelBytes, 1024),
-                                idPV, (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      // Phases across items: gk key tiles so far (the K/V ring), c_t scores of
-      // tile t so far (SFull_t and PFull_t), ti items (the Q buffers).
-      int gk = 0, c0 = 0, c1 = 0, ti = 0;
-      bool ok = true;
-      if constexpr (L::kSplitP) {
-        // Split Pbar: per key tile j, S_0(j) and S_1(j) (each once its softmax
-        // holds the previous scores of its tile), then the products of key tile
-        // j - 1 with each tile's Pbar. The scores of the next key tile are thus
-        // computed while the softmax works on the current one.
-        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
-          const Item it = decode(item);
-          const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
-          const int qb = ti % L::kQBufs;
-          if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
-          for (int j = 0; ok && j <= n_iter; ++j) {
-            if (j < n_iter) {
-              const int s = (gk + j) % L::kStages;
-              if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
-              if (lane == 0) PFA_FWD_TRACE(0, 1, j);
-              if (j <= last0) {
-                if (c0 + j > 0 && !(ok = wait_warp(bar(L::bSFree + 0), (c0 + j - 1) & 1, ctl))) break;
-                tc_fence_after();
-                issue_s(0, qb, s);
-              }
-              if (j <= last1) {
-                if (c1 + j > 0 && !(ok = wait_warp(bar(L::bSFree + 1), (c1 + j - 1) & 1, ctl))) break;
-                tc_fence_after();
-                issue_s(1, qb, s);
-              }
-            }
-            if (j > 0) {
-              const int jp = j - 1;
-              const int sp = (gk + jp) % L::kStages;
-              if (jp <= last0) {
-                if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + jp) & 1, ctl))) break;
-                if (lane == 0) PFA_FWD_TRACE(0, 3, jp);
-                tc_fence_after();
-                issue_pv(0, sp, jp);
-                umma_commit_warp(bar(L::bPVDone + 0));
-                if (jp == last0) umma_commit_warp(bar(L::bODone + 0));
-              }
-              if (jp <= last1) {
-                if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + jp) & 1, ctl))) break;
-                if (lane == 0) PFA_FWD_TRACE(0, 2, jp);
-                tc_fence_after();
-                issue_pv(1, sp, jp);
-                umma_commit_warp(bar(L::bPVDone + 1));
-                if (jp == last1) umma_commit_warp(bar(L::bODone + 1));
-              }
-              umma_commit_warp(bar(L::bKVEmpty + sp));
-            }
-          }
-          // The item's products are done once this arrives: its Q buffer is free.
-          umma_commit_warp(bar(L::bQEmpty + qb));
-          gk += n_iter;
-          c0 += last0 + 1;
-          c1 += last1 + 1;
-        }
-      } else {
-      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
-        const Item it = decode(item);
-        const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
-        const int qb = ti % L::kQBufs;
-        if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
-        for (int j = 0; ok && j < n_iter; ++j) {
-          const int s = (gk + j) % L::kStages;
-          if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
-          const bool act0 = j <= last0, act1 = j <= last1;
-          if (lane == 0) PFA_FWD_TRACE(0, 1, j);
-          tc_fence_after();
-          if (act0) issue_s(0, qb, s);
-          if (j > 0 && j - 1 <= last1) {
-            if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + j - 1) & 1, ctl))) break;
-            if (lane == 0) PFA_FWD_TRACE(0, 2, j - 1);
-            tc_fence_after();
-            const int sp = (gk + j - 1) % L::kStages;
-            issue_pv(1, sp, j - 1);
-            umma_commit_warp(bar(L::bKVEmpty + sp));
-            if (j - 1 == last1) umma_commit_warp(bar(L::bODone + 1));
-          }
-          if (act1) issue_s(1, qb, s);
-          if (act0) {
-            if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + j) & 1, ctl))) break;
-            if (lane == 0) PFA_FWD_TRACE(0, 3, j);
-            tc_fence_after();
-            issue_pv(0, s, j);
-            if (j == last0) umma_commit_warp(bar(L::bODone + 0));
-            if (!act1) umma_commit_warp(bar(L::bKVEmpty + s));
-          }
-        }
-        if (ok && last1 == n_iter - 1) {
-          const int j = n_iter - 1;
-          if ((ok = wait_warp(bar(L::bPFull + 1), (c1 + j) & 1, ctl))) {
-            tc_fence_after();
-            issue_pv(1, (gk + j) % L::kStages, j);
-            umma_commit_warp(bar(L::bKVEmpty + (gk + j) % L::kStages));
-            umma_commit_warp(bar(L::bODone + 1));
-          }
-        }
-        // The item's products are done once this arrives: its Q buffer is free.
-        umma_commit_warp(bar(L::bQEmpty + qb));
-        gk += n_iter;
-        c0 += last0 + 1;
-        c1 += last1 + 1;
-      }
-      }
-      // Drain: no MMA may still read shared memory or write TMEM at teardown.
-      umma_commit_warp(bar(L::bDrain));
-      wait_drain(bar(L::bDrain), 0, ctl);
-    }
-    }
-    __syncwarp();
-    // Reclaim registers only after both compute warpgroups have taken theirs:
-    // otherwise an early exit of this group could take the registers they are
-    // waiting for. Their arrival follows their first instruction, so this wait is
-    // short; it is bounded like every other wait.
-    wait_drain(bar(L::bRegs), 0, ctl);
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
-  } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(L::bRegs));
-    if (*abort_flag == 0) {
-      // ---------------- softmax warps ----------------
-      const int t = (warp - 4) >> 2;  // query tile of this warpgroup
-      const uint32_t quarter = warp & 3;
-      const int r = quarter * 32 + lane;  // row within the tile == TMEM lane
-      const uint32_t lane_off = (quarter * 32u) << 16;
-      const uint32_t tS = tmem + 128 * t + lane_off;
-      const uint32_t tO = tmem + 256 + D * t + lane_off;
-      const uint32_t tP = L::kSplitP ? tmem + L::kColP + 64 * t + lane_off : tS;   // Pbar_t
-      const float sl2 = sh.scale_log2;
-      const float alpha = sh.scale;
-
-      // Shift rule (paper §4 equation; Algorithm 1): only rows whose maximum
-      // repeats within eps change their shift.
-      auto shift_of = [&](float mx, bool repeated) {
-        const float r_m = mx * alpha;
-        if (MODE == 0 || !repeated) return r_m;
-        if (MODE == 1) return r_m > 0.f ? args.beta * r_m : (r_m < 0.f ? 0.f : kEpsShift);
-        return r_m + kEpsShift;
-      };
-      bool ok = true;
-      int ct = 0, ot = 0;   // phases across items: scores of this tile, items with this tile
-      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
-      const Item itm = decode(item);
-      const int last = t ? itm.last1 : itm.last0;
-      if (last < 0) continue;             // the pair has no second tile
-      const int bh = itm.bh;
-      const int q0 = (itm.qt0 + t) * kTile;
-      const int qrow = q0 + r;
-      float m1 = -INFINITY;                  // running maximum of raw scores
-      bool rep = false;                      // two entries within eps of m1
-      float m_sh = -INFINITY;                // current shift, natural units
-      float l0 = 0.f, l1 = 0.f;              // row sum of Pbar (two partial sums)
-      int cnt = 0;                           // entries within tau of m1 (raw)
-
-      for (int j = 0; j <= last; ++j) {
-        const int k0 = j * kTile;
-        const bool need_mask = (CAUSAL && k0 + kTile > q0) || (k0 + kTile > N);
-        if (!(ok = wait_warp(bar(L::bSFull + t), (ct + j) & 1, ctl))) break;
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 4, j);
-        tc_fence_after();
-        uint32_t v[128];
-        tmem_ld64(tS, v);
-        tmem_ld64(tS + 64, v + 64);
-        tmem_ld_wait64(v);
-        tmem_ld_wait64(v + 64);
-        if constexpr (L::kSplitP) {
-          // The scores are in registers: the next S_t may overwrite them.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::bSFree + t));
-        }
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            const int key = k0 + c;
-            if (!(key < N && (!CAUSAL || key <= qrow))) v[c] = __float_as_uint(-INFINITY);
-          }
-        }
-        // Tile maximum, as the maxima of eight blocks of 16 columns.
-        float bm[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          auto x = [&](int e) { return __uint_as_float(v[16 * k + e]); };
-          const float u0 = fmax3(x(0), x(1), x(2)), u1 = fmax3(x(3), x(4), x(5));
-          const float u2 = fmax3(x(6), x(7), x(8)), u3 = fmax3(x(9), x(10), x(11));
-          const float u4 = fmax3(x(12), x(13), x(14));
-          bm[k] = fmaxf(fmax3(u0, u1, u2), fmax3(u3, u4, x(15)));
-        }
-        const float t1 = fmax3(fmax3(bm[0], bm[1], bm[2]), fmax3(bm[3], bm[4], bm[5]), fmaxf(bm[6], bm[7]));
-        // Repetition flag of the running row (at least two entries within eps of
-        // its maximum), kept exactly tile by tile without a second maximum:
-        //   new maximum t1 > m1: repeated iff m1 >= t1 - eps or this tile holds two
-        //                        entries >= t1 - eps;
-        //   m1 - eps <= t1 <= m1: repeated (an entry of this tile ties the maximum);
-        //   otherwise the flag is unchanged.
-        // Two entries of the tile reach a threshold iff two of the eight 16-column
-        // blocks do or two of the sixteen column classes (column mod 16) do: a
-        // single qualifying entry lies in one block and one class, and two
-        // distinct entries differ in their block or in their class. The block
-        // count is known with the maximum; the class maxima are gathered during
-        // the exponentials. A new maximum alone in its block is taken as single
-        // until they show otherwise, and a row found repeated then has its tile
-        // recomputed under the repeated shift (a second pass, taken only when a
-        // tie sits inside one block of a new maximum).
-        bool jump = false;
-        int nb = 0;
-        float thr_eps = 0.f;
-        bool rep_use = rep;
-        if (kTies) {
-          thr_eps = t1 - args.eps_raw;
-          jump = t1 > m1 && m1 < thr_eps;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) nb += bm[k] >= thr_eps ? 1 : 0;
-          if (t1 > m1) {
-            rep_use = jump ? nb >= 2 : true;
-          } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
-            rep_use = true;
-          }
-        }
-        const float m1_old = m1;
-        m1 = fmaxf(m1, t1);
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 5, j);
-
-        // Pbar = exp(S - m) in FP32; l sums it; the BF16 casts go to TMEM.
-        const float l0s = l0, l1s = l1;
-        float m_new = m_sh, corr = 1.f;
-        bool changed = false;
-        int cnt_tile = 0;
-#pragma unroll 1
-        for (int pass = 0;; ++pass) {
-          m_new = shift_of(m1, rep_use);
-          changed = (j > 0) && (m_new != m_sh);
-          corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
-          l0 = l0s * corr;
-          l1 = l1s * corr;
-          const float nml2 = -m_new * kLog2e;
-          const float thr = m1 - args.tau_raw;
-          cnt_tile = 0;
-          float ce[16];   // class maxima (column mod 16)
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int u = 0; u < 32; ++u) {
-              const float x0 = __uint_as_float(v[64 * half + 2 * u]);
-              const float x1 = __uint_as_float(v[64 * half + 2 * u + 1]);
-              if (COUNT) cnt_tile += (x0 >= thr) + (x1 >= thr);
-              float y0, y1;
-              fma2(y0, y1, x0, x1, sl2, nml2);
-              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-              add2(l0, l1, p0, p1);
-              pk[u] = pack_bf16x2(p0, p1);
-            }
-            if (kTies) {
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                auto x = [&](int k) { return __uint_as_float(v[64 * half + 16 * k + e]); };
-                const float c4 = fmaxf(fmax3(x(0), x(1), x(2)), x(3));
-                ce[e] = half ? fmaxf(ce[e], c4) : c4;
-              }
-            }
-            if constexpr (L::kSplitP) {
-              // Obar_t and the Pbar_t columns are free once the previous key
-              // tile's product has completed (tile 0 of an item: its epilogue
-              // waited for the last product of the previous item). Without split
-              // Pbar, S_t of this tile was committed after that product.
-              // A failed wait ends the loop at the bottom of this iteration.
-              if (half == 0 && pass == 0 && j > 0) {
-                ok = wait_warp(bar(L::bPVDone + t), (ct + j - 1) & 1, ctl);
-                tc_fence_after();
-              }
-            }
-            tmem_st32(tP + 32 * half, pk);
-          }
-          if (!kTies || pass > 0) break;
-          const bool single = jump && nb < 2;
-          if (!__any_sync(0xFFFFFFFFu, single)) break;
-          int ne = 0;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) ne += ce[e] >= thr_eps ? 1 : 0;
-          const bool wrong = single && ne >= 2;
-          if (wrong) rep_use = true;
-          // Mode 0 keeps the flag for the counter only: its shift does not move.
-          if (MODE == 0 || !__any_sync(0xFFFFFFFFu, wrong)) break;
-          tmem_st_wait();   // the second pass stores over the first one's Pbar
-        }
-        rep = rep_use;
-        m_sh = m_new;
-        if (COUNT) cnt = (m1 - m1_old > args.tau_raw) ? cnt_tile : cnt + cnt_tile;
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 6, j);
-        // Rescale Obar where the shift moved: the scores are dead, so one TMEM
-        // round trip covers 64 columns.
-        if (__any_sync(0xFFFFFFFFu, changed)) {
-#pragma unroll 1
-          for (int c = 0; c < D; c += 64) {
-            uint32_t o[64];
-            tmem_ld64(tO + c, o);
-            tmem_ld_wait64(o);
-#pragma unroll
-            for (int u = 0; u < 64; u += 2) {
-              float y0 = __uint_as_float(o[u]), y1 = __uint_as_float(o[u + 1]);
-              mul2(y0, y1, corr);
-              o[u] = __float_as_uint(y0);
-              o[u + 1] = __float_as_uint(y1);
-            }
-            tmem_st64(tO + c, o);
-          }
-        }
-        tmem_st_wait();
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 7, j);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(bar(L::bPFull + t));
-
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 8, j);
-        if (!ok) break;
-      }
-
-      // ---------------- epilogue ----------------
-      if (ok) ok = wait_warp(bar(L::bODone + t), ot & 1, ctl);
-      if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 9, ot);
-      if (ok) {
-        tc_fence_after();
-        // The flag is exact after every tile, so the shift in use is the final one.
-        const float m_fin = m_sh;
-        const float l = l0 + l1;
-        const bool row_ok = qrow < N;
-        const float inv_l = 1.f / l;
-        __nv_bfloat16* orow =
-            reinterpret_cast<__nv_bfloat16*>(args.o) + (static_cast<size_t>(bh) * N + qrow) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(tO + c, o);
-          tmem_ld_wait32(o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float y0 = __uint_as_float(o[2 * u]), y1 = __uint_as_float(o[2 * u + 1]);
-            mul2(y0, y1, inv_l);
-            pk[u] = pack_bf16x2(y0, y1);
-          }
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int qd = 0; qd < 4; ++qd)
-              dst[qd] = make_uint4(pk[4 * qd], pk[4 * qd + 1], pk[4 * qd + 2], pk[4 * qd + 3]);
-          }
-        }
-        if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 10, ot);
-        if (row_ok) args.lse[static_cast<size_t>(bh) * N + qrow] = m_fin + lg2_approx(l) * kLn2;
-        if (COUNT) {
-          // BF16(Pbar) == 1 under the final shift: entries within tau of m1,
-          // unless the shift moved the maximum more than tau below zero.
-          const float moved = m_fin - m1 * alpha;
-          long long c_rep = row_ok && rep ? 1 : 0;
-          long long c_one = row_ok && moved <= args.tau_raw * alpha ? cnt : 0;
-          long long c_nf = row_ok && !(l > 0.f && l < INFINITY) ? 1 : 0;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            c_rep += __shfl_xor_sync(0xFFFFFFFFu, c_rep, o);
-            c_one += __shfl_xor_sync(0xFFFFFFFFu, c_one, o);
-            c_nf += __shfl_xor_sync(0xFFFFFFFFu, c_nf, o);
-          }
-          if (lane == 0 && args.counters) {
-            if (c_rep) atomicAdd(reinterpret_cast<unsigned long long*>(args.counters + 0),
-                                 static_cast<unsigned long long>(c_rep));
-            if (c_one) atomicAdd(reinterpret_cast<unsigned long long*>(args.counters + 1),
-                                 static_cast<unsigned long long>(c_one));
-            if (c_nf) atomicAdd(reinterpret_cast<unsigned long long*>(args.counters + 2),
-                                static_cast<unsigned long long>(c_nf));
-          }
-        }
-      }
-      ct += last + 1;
-      ++ot;
-      }
-    }
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 168;" ::: "memory");
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-template <int D, int MODE, bool CAUSAL, bool COUNT>
-cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& a, cudaStream_t stream) {
-  using L = FwdLayout<D>;
-  auto kern = attn_fwd_kernel<D, MODE, CAUSAL, COUNT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
-  if (e != cudaSuccess) return e;
-  // Persistent: one CTA per SM (at most one per work item).
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const int n_kt = (a.s.N + kTile - 1) / kTile;
-  const long long n_items = static_cast<long long>((n_kt + 1) / 2) * a.s.B * a.s.Hq;
-  const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, a);
-}
 
 template <int D, int MODE>
 cudaError_t dispatch_causal(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& a, cudaStream_t st) {
   const bool count = a.counters != nullptr;
   if (a.s.causal)
-    return count ? launch_fwd_t<D, MODE, true, true>(tq, tk, tv, a, st)
-                 : launch_fwd_t<D, MODE, true, false>(tq, tk, tv, a, st);
-  return count ? launch_fwd_t<D, MODE, false, true>(tq, tk, tv, a, st)
-               : launch_fwd_t<D, MODE, false, false>(tq, tk, tv, a, st);
+    return count ? fwd::launch_fwd_t<D, MODE, true, 1, false>(tq, tk, tv, a, st)
+                 : fwd::launch_fwd_t<D, MODE, true, 0, false>(tq, tk, tv, a, st);
+  return count ? fwd::launch_fwd_t<D, MODE, false, 1, false>(tq, tk, tv, a, st)
+               : fwd::launch_fwd_t<D, MODE, false, 0, false>(tq, tk, tv, a, st);
 }
 
 template <int D>

@@ -53,12 +53,14 @@ struct FwdArgs {
   void* o;                 // bf16 [B, Hq, N, d]
   float* lse;              // [B, Hq, N]
   long long* counters;     // 3 x int64 or null
+  long long* monitor;      // 1 + 8 x int64 (operational ones, tie histogram) or null
   int* err;                // device error word
   unsigned long long* err_site;  // where the first bounded wait gave up
   int fix_mode;
   float beta;
   float eps_raw;           // tie tolerance in units of the unscaled score Q.K
   float tau_raw;           // BF16 round-to-one window in units of Q.K
+  int profile;             // the unfused BF16 Pbar V study profile (d = 64)
 };
 
 struct DeltaAltArgs {
@@ -93,6 +95,10 @@ struct DqArgs {
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, cudaStream_t stream);
+// The forward kernel's study variants: the monitor (a.monitor) and the unfused
+// BF16 profile (a.profile, d = 64); counters as in launch_fwd.
+cudaError_t launch_fwd_study(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long rows, int d,
                          cudaStream_t stream);
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -29,7 +29,7 @@ from dataclasses import dataclass, field
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "make", "gaussian", "integer_grid", "signed_max_grid",
-           "sink_heavy", "large_logit_rows", "underflow_probe"]
+           "sink_heavy", "tie_probe", "large_logit_rows", "underflow_probe"]
 
 
 @dataclass(frozen=True)
@@ -227,6 +227,34 @@ def sink_heavy(B=4, H=12, N=2048, d=64, *, seed=0, dup_frac=0.10) -> dict:
                 if jp >= js:
                     jp += 1
                 k[b, h, jp] = k[b, h, js]
+    return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
+            "v": v.to(torch.bfloat16).contiguous(), "do": do.to(torch.bfloat16).contiguous()}
+
+
+def tie_probe(B=1, H=12, N=1024, d=64, *, ties=2, logit=16.0, seed=0) -> dict:
+    """Rows whose maximum is a sink key repeated ``ties`` times (scale 1/8).
+
+    * base Q, K ~ N(0, 0.25), dO ~ N(0, 1e-4);
+    * key 0 carries an exact +``logit`` (feature d-1 reserved: Q[..., d-1] = 1,
+      K[..., 0, d-1] = logit * 8, K[..., j>0, d-1] = 0), and keys 1 .. ties-1 are copies of
+      key 0, so every row i >= ties - 1 has exactly ``ties`` tied maxima; with a logit of 16
+      the other keys' weights are e^-16 each, so their sum stays far below a BF16 spacing
+      of the output;
+    * V feature f ~ N(mu_f, 0.25) with mu_f ~ N(-1, 0.01): negative-dominated features.
+    """
+    g = _gen(seed)
+    q = _normal((B, H, N, d), 0.5, g)
+    k = _normal((B, H, N, d), 0.5, g)
+    mu = _normal((B, H, 1, d), 0.1, g, mean=-1.0)
+    v = _normal((B, H, N, d), 0.5, g) + mu
+    do = _normal((B, H, N, d), 1e-2, g)
+    q = q.to(torch.bfloat16).float()
+    k = k.to(torch.bfloat16).float()
+    q[..., d - 1] = 1.0
+    k[..., d - 1] = 0.0
+    k[..., 0, d - 1] = logit * 8.0
+    for t in range(1, ties):
+        k[..., t, :] = k[..., 0, :]
     return {"q": q.to(torch.bfloat16).contiguous(), "k": k.to(torch.bfloat16).contiguous(),
             "v": v.to(torch.bfloat16).contiguous(), "do": do.to(torch.bfloat16).contiguous()}
 

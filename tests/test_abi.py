@@ -166,3 +166,22 @@ def test_bwd_ex_validates(lib):
         bad = list(args)
         bad[17], bad[9] = 2, None        # with the query-outer pass dq_accum may be NULL
         assert lib.pfa_attn_bwd_ex(*bad) not in (inv, mis)
+
+
+def test_fwd_ex_validates(lib):
+    inv, mis = -1, -2
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, Hq=2, Hkv=1, N=64, d=64, causal=0, scale=0.125,
+                mode=0, beta=2.0, eps=1e-3, counters=None, monitor=None, flags=0, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return lib.pfa_attn_fwd_ex(*a.values())
+
+    assert call(flags=2) == inv                       # an unknown flag bit
+    assert call(monitor=A + 4) == mis                 # the monitor must be 8-byte aligned
+    assert call(monitor=A, eps=-1.0) == inv           # the monitor needs a valid eps
+    assert call(q=None) == inv
+    if _no_device():
+        assert call(flags=1, d=128) == -3             # the unfused profile is d = 64 only
+        assert call(flags=1) not in (inv, mis)

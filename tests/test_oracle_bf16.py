@@ -3,6 +3,8 @@ import math
 import os
 
 import numpy as np
+
+import oracle
 import pytest
 import torch
 
@@ -104,3 +106,55 @@ def test_ftz():
     assert y[0] == 0 and y[1] == 0 and np.signbit(y[1])
     assert y[2] == np.float32(2.0 ** -126) and y[3] == np.float32(-(2.0 ** -126))
     assert y[5] == 1.0
+
+
+# ---------------------------------------------------------------- narrower formats
+def test_e4m3_matches_the_library_cast_in_range():
+    import torch
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(200000) * 10.0 ** rng.uniform(-4, 2.5, 200000),
+                        rng.uniform(-440, 440, 20000), [0.0, -0.0, 1.0, 0.96875, 2.0 ** -9,
+                                                        2.0 ** -10, 3 * 2.0 ** -11, 448.0]])
+    x32 = x.astype(np.float32)
+    x32 = x32[np.abs(x32) <= 448.0]   # the library cast gives NaN beyond the range; we saturate
+    lib = torch.from_numpy(x32).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_rne(x32.astype(np.float64)), lib)
+
+
+def test_e4m3_special_cases():
+    # 1 - 2^-5 is the midpoint between 0.9375 and 1 and ties to the even 1.0: the mode-2 shift
+    # exp(-2^-5) = 0.969 rounds back to exactly one in E4M3.
+    assert oracle.e4m3_rne(1 - 2.0 ** -5) == 1.0
+    assert oracle.e4m3_rne(float(np.exp(-2.0 ** -5))) == 1.0
+    assert oracle.e4m3_rne(0.95) == 0.9375
+    assert oracle.e4m3_rne(1000.0) == 448.0 and oracle.e4m3_rne(-1e9) == -448.0
+    assert oracle.e4m3_rne(2.0 ** -10) == 0.0      # half the smallest subnormal: ties to zero
+    assert oracle.e4m3_rne(3 * 2.0 ** -11) == 2.0 ** -9
+
+
+def test_e2m1_is_the_nearest_grid_value_ties_to_even():
+    grid = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    even = {0: True, 0.5: False, 1: True, 1.5: False, 2: True, 3: False, 4: True, 6: True}
+    rng = np.random.default_rng(1)
+    x = np.concatenate([rng.uniform(0, 7, 5000), (grid[1:] + grid[:-1]) / 2])
+    for v in x:
+        d = np.abs(grid - v)
+        best = grid[d == d.min()]
+        want = best[0] if len(best) == 1 else [b for b in best if even[float(b)]][0]
+        want = min(want, 6.0) if v <= 6 else 6.0
+        assert oracle.e2m1_rne(v) == want, v
+        assert oracle.e2m1_rne(-v) == -want
+
+
+def test_mx_e2m1_block_scales():
+    # A block whose largest magnitude is 1 gets the scale 2^-2, so 1 -> 4 X = 1 exactly and
+    # 0.97 -> 3.88 X -> 4 X = 1: near-ones round to one. Blocks are 32 elements long.
+    x = np.zeros(64)
+    x[0], x[1], x[2] = 1.0, 0.97, 0.3
+    x[32], x[33] = 0.01, 0.004
+    q = oracle.mx_e2m1(x)
+    assert q[0] == 1.0 and q[1] == 1.0 and q[2] == 0.25
+    # second block: amax 0.01 -> floor(log2 0.01) = -7, X = 2^-9; 0.01 / X = 5.12 -> 6 (nearest
+    # of 4 and 6 is 6); 0.004 / X = 2.048 -> 2
+    assert q[32] == 6 * 2.0 ** -9 and q[33] == 2 * 2.0 ** -9
+    assert np.all(q[34:] == 0)

@@ -145,8 +145,11 @@ def test_nonpositive_repeated_maxima(mode, sign, causal, d):
         e_emu = rel_l2(e["dq"], full["dq"][0])
         e_gpu = rel_l2(got["dq"][0], full["dq"][0])
         assert e_gpu <= max(TOL_BWD_REL, 1.5 * e_emu), (e_gpu, e_emu)
-        split = run_gpu(t, dq_mode="split", **kw)
-        assert_bwd_close(split, full, "signed maxima (split dS)")
+        # With the query-outer pass the remaining error is delta's: rowsum(dO o O) from the
+        # BF16 O moves dQ by percent here (the pages' point: the error enters through delta),
+        # rowsum(dP o P) does not.
+        split = run_gpu(t, dq_mode="split", delta_mode=1, **kw)
+        assert_bwd_close(split, full, "signed maxima (split dS, delta from dP o P)")
 
 
 # ---------------------------------------------------------------- ragged shapes
