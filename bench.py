@@ -279,6 +279,12 @@ class Step:
         self.pfa.attn_bwd(t["q"], t["k"], t["v"], t["do"], self.lse, self.delta, self.dq, self.dk,
                           self.dv, self.ws, **self.kw)
 
+    def bwd_ex(self, flags):
+        """The backward call with pfa_attn_bwd_ex options (the query-outer dQ pass)."""
+        t = self.t
+        self.pfa.attn_bwd_ex(t["q"], t["k"], t["v"], t["do"], self.lse, self.delta, self.dq, self.dk,
+                             self.dv, None, flags=flags, **self.kw)
+
     def bwd_kernel(self):
         """The backward kernel alone (pfa_attn_bwd_accum into the zeroed FP32 workspace)."""
         t = self.t
@@ -339,6 +345,8 @@ def time_step(step, steps, warmup, flush, split=False):
 
         out["bwd_kernel_ms"] = alone(step.bwd_kernel, step.ws.zero_)
         out["delta_alt_ms"] = alone(step.delta_alt_)
+        out["bwd_det_ms"] = alone(lambda: step.bwd_ex(1))
+        out["bwd_split_ms"] = alone(lambda: step.bwd_ex(3))
     return out
 
 
@@ -384,6 +392,11 @@ def measure_workload(name, device, steps, flush, peaks):
             e[k + "_frac_bf16_peak"] = e[k + "_tflops"] / peak
         e["delta_alt_ms"] = med["delta_alt_ms"]
         e["delta_alt_tflops"] = f_alt / med["delta_alt_ms"] / 1e9
+        # The backward call with the query-outer dQ pass: deterministic dQ, and with the hi/lo
+        # BF16 dS (algorithmic FLOPs as above; the pass recomputes S and dP).
+        for k in ("det", "split"):
+            e[f"bwd_{k}_ms"] = med[f"bwd_{k}_ms"]
+            e[f"bwd_{k}_tflops"] = f_bwd / med[f"bwd_{k}_ms"] / 1e9
         if name != "sink":
             e["delta_ms"] = med["delta_ms"]
             e["delta_gbs"] = dl_bytes / med["delta_ms"] / 1e6

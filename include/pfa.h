@@ -134,11 +134,24 @@ typedef struct pfa_monitor {
                                       in BF16 computes O ([PK] caveats: the analysed code
                                       keeps P V in BF16). Not a fast path. */
 
+#define PFA_FWD_PBAR_E4M3 2u         /* study, d = 64: Pbar is rounded to FP8 E4M3 (nearest,
+                                        ties to even, saturating) before the Pbar V product */
+#define PFA_FWD_PBAR_MXFP4 4u        /* study, d = 64: Pbar is rounded to MXFP4: E2M1 values
+                                        with one power-of-two scale 2^(floor(log2 amax) - 2)
+                                        per 32 consecutive keys. With either narrow format l
+                                        sums the rounded values (the weights the product
+                                        uses); the rounded values are exact in BF16, so the
+                                        BF16 product with FP32 accumulation computes what a
+                                        product in that format does. The pages leave open how
+                                        the bias behaves with fewer mantissa bits ([PK] open
+                                        questions). Combine with PFA_FWD_UNFUSED_BF16_PV for the
+                                        paper's profile; not with each other. */
+
 /* pfa_attn_fwd with the monitor and options (no counterpart in the paper).
  * counters and monitor are optional (NULL); flags 0 and monitor NULL is
- * pfa_attn_fwd exactly. PFA_FWD_UNFUSED_BF16_PV with d != 64 returns
- * PFA_ERR_UNSUPPORTED; unknown flag bits PFA_ERR_INVALID_ARG. eps must be finite
- * and >= 0 when a monitor is given. */
+ * pfa_attn_fwd exactly. The study flags with d != 64 return PFA_ERR_UNSUPPORTED;
+ * unknown flag bits, or both narrow formats, PFA_ERR_INVALID_ARG. eps must be
+ * finite and >= 0 when a monitor is given. */
 int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
                     int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
                     float beta, float eps, pfa_counters* counters, pfa_monitor* monitor,
@@ -164,7 +177,11 @@ int pfa_attn_delta_alt(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
  *   q, dO [B,H_q,N,d], k, v [B,H_kv,N,d], lse, delta [B,H_q,N] (in);
  *   dq [B,H_q,N,d], dk, dv [B,H_kv,N,d] (out, BF16);
  *   dq_accum: FP32 workspace of pfa_bwd_workspace_bytes() bytes, caller-owned
- *   device memory; its contents on entry are ignored (it is zeroed on `stream`). */
+ *   device memory; its contents on entry are ignored (it is zeroed on `stream`).
+ * At d = 64 the key-outer kernel reduce-adds each key tile's dQ into the
+ * workspace, which is then converted to BF16. At d = 128 dQ comes from the
+ * query-outer pass of pfa_attn_bwd_ex (PFA_BWD_DQ_DETERMINISTIC), which is faster
+ * there; the workspace is then not touched. */
 int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
                  const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
                  float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,

@@ -18,13 +18,13 @@ the three fix modes, the delta identity, central finite differences of the
 backward pass, and brute-force counts on integer-valued inputs.
 """
 from .attention import (EPS_SHIFT, TIE_BINS, attn_bwd, attn_bwd_rows, attn_delta, attn_delta_alt, attn_fwd,
-                        attn_fwd_head, attn_fwd_monitor, attn_fwd_unfused, fix_shift, scores,
+                        attn_fwd_blockwise, attn_fwd_head, attn_fwd_monitor, attn_fwd_unfused, fix_shift, scores,
                         visible)
 from .bf16 import (BF16_ONE_THRESHOLD, E2M1_MAX, E4M3_MAX, MX_BLOCK, bf16_rne, bf16_sum, e2m1_rne,
                    e4m3_rne, fp32, ftz32, mx_e2m1)
 
 __all__ = [
-    "EPS_SHIFT", "TIE_BINS", "attn_bwd", "attn_bwd_rows", "attn_fwd_monitor", "attn_fwd_unfused", "attn_delta", "attn_delta_alt", "attn_fwd", "attn_fwd_head",
+    "EPS_SHIFT", "TIE_BINS", "attn_bwd", "attn_bwd_rows", "attn_fwd_monitor", "attn_fwd_unfused", "attn_fwd_blockwise", "attn_delta", "attn_delta_alt", "attn_fwd", "attn_fwd_head",
     "fix_shift", "scores", "visible", "BF16_ONE_THRESHOLD", "bf16_rne", "bf16_sum", "fp32",
     "ftz32", "E2M1_MAX", "E4M3_MAX", "MX_BLOCK", "e2m1_rne", "e4m3_rne", "mx_e2m1",
 ]

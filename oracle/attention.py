@@ -58,7 +58,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .bf16 import bf16_rne, fp32, ftz32
+from .bf16 import bf16_rne, e4m3_rne, fp32, ftz32, mx_e2m1
 
 __all__ = [
     "EPS_SHIFT",
@@ -73,6 +73,7 @@ __all__ = [
     "attn_bwd_rows",
     "attn_fwd_monitor",
     "attn_fwd_unfused",
+    "attn_fwd_blockwise",
     "TIE_BINS",
 ]
 
@@ -370,22 +371,46 @@ def attn_fwd_unfused(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0,
     """The forward pass as an implementation that stores the unnormalised product Pbar V in
     BF16 computes it: the paper's analysed code, FlashAttention 2 written as PyTorch
     operations with blocks of 512 keys (PK "의심해볼 점"; the bias mechanism of PK
-    "핵심 아이디어", paper §3.3.2, and BN "Results", Fig. 6).
+    "핵심 아이디어", paper §3.3.2, and BN "Results", Fig. 6). :func:`attn_fwd_blockwise`
+    with a BF16 Pbar and BF16 accumulation."""
+    return attn_fwd_blockwise(q, k, v, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta,
+                              eps=eps, block=block, pbar="bf16", accumulate="bf16")
+
+
+def _round_pbar(p32, pbar):
+    """The Pbar operand: BF16, FP8 E4M3, or MXFP4 (E2M1 with one power-of-two scale per 32
+    consecutive keys, :func:`oracle.bf16.mx_e2m1`), from the FP32 Pbar of one key block."""
+    if pbar == "bf16":
+        return ftz32(bf16_rne(p32)).astype(np.float64)
+    if pbar == "e4m3":
+        return e4m3_rne(p32)
+    if pbar == "mxfp4":
+        return mx_e2m1(p32, axis=-1)
+    raise ValueError("pbar must be 'bf16', 'e4m3' or 'mxfp4'")
+
+
+def attn_fwd_blockwise(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3,
+                       block=128, pbar="bf16", accumulate="bf16") -> dict:
+    """Blockwise online softmax with a chosen Pbar format and Obar precision.
 
     Per row, per ``block`` of keys in order: the running maximum and the repetition flag of
-    the keys so far give the shift m_b (:func:`fix_shift`); Pbar = BF16(exp(S - m_b)) from an
-    FP32 exponential (flushed to zero below the normal range); the block's product
-    U_b = BF16(sum_j Pbar_j V_j) is formed exactly and rounded once (an FP32-accumulating
-    BF16 matrix product with a BF16 result, the accumulation model of the pages' worked
-    traces, :func:`oracle.bf16.bf16_sum`); the accumulator follows
-    Obar = BF16(BF16(Obar * c_b) + U_b) with c_b = exp(m_(b-1) - m_b) in FP32; l = FP32
-    (l * c_b + sum of the BF16 Pbar) -- the normaliser sums the weights the product used (a
-    reading: the pages name only P V as stored in BF16). Finally O = BF16(Obar / l) and
-    lse = m + ln l (FP32). Scores are FP32 (one rounding of the exact dot, times FP32 alpha).
+    the keys so far give the shift m_b (:func:`fix_shift`); Pbar = ``pbar``(exp(S - m_b)) from
+    an FP32 exponential (flushed to zero below the normal range); the block's product
+    U_b = sum_j Pbar_j V_j is formed exactly and, with ``accumulate="bf16"``, rounded once to
+    BF16 (an FP32-accumulating matrix product with a BF16 result, the accumulation model of
+    the pages' worked traces, :func:`oracle.bf16.bf16_sum`) and accumulated as
+    Obar = BF16(BF16(Obar * c_b) + U_b); with ``accumulate="fp32"``, Obar = FP32(Obar * c_b +
+    U_b). c_b = exp(m_(b-1) - m_b) in FP32. l = FP32(l * c_b + sum of the rounded Pbar): the
+    normaliser sums the weights the product used (a reading: the pages name only P V as
+    stored in BF16). Finally O = BF16(Obar / l) and lse = m + ln l (FP32). Scores are FP32 (one
+    rounding of the exact dot, times FP32 alpha).
 
-    Returns ``o``, ``lse`` [B,H_q,N,d] / [B,H_q,N] and ``obar`` (the BF16 accumulator before
-    normalisation)."""
+    ``pbar`` "e4m3" and "mxfp4" are the narrower formats whose effect the pages leave open
+    (PK "열린 질문"). Returns ``o``, ``lse``, ``obar`` (the accumulator before normalisation)
+    and ``operational_ones`` (rounded Pbar entries equal to 1.0 handed to the products)."""
     B, Hq, Hkv, N, d = _check_shapes(q, k, v)
+    if accumulate not in ("bf16", "fp32"):
+        raise ValueError("accumulate must be 'bf16' or 'fp32'")
     group = Hq // Hkv
     if scale is None:
         scale = 1.0 / np.sqrt(d)
@@ -394,6 +419,7 @@ def attn_fwd_unfused(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0,
     o = np.zeros(q.shape)
     obar_all = np.zeros(q.shape)
     lse = np.zeros((B, Hq, N))
+    ones = 0
     for b in range(B):
         for h in range(Hq):
             kv = h // group
@@ -412,14 +438,19 @@ def attn_fwd_unfused(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0,
                     c = np.where(np.isfinite(m_prev), ftz32(np.exp(fp32(m_prev - m))), 0.0)
                 with np.errstate(invalid="ignore"):
                     x = np.where(live[:, None], s[:, j0: j0 + block] - m[:, None], -np.inf)
-                pbar = ftz32(bf16_rne(ftz32(np.exp(fp32(x)))))
-                l = fp32(l.astype(np.float64) * c + pbar.astype(np.float64).sum(axis=1))
-                u = bf16_rne(fp32(pbar.astype(np.float64) @ v[b, kv, j0: j0 + block]))
-                scaled = bf16_rne(fp32(obar.astype(np.float64) * c[:, None]))
-                obar = bf16_rne(fp32(scaled.astype(np.float64) + u.astype(np.float64)))
+                p = _round_pbar(ftz32(np.exp(fp32(x))), pbar)
+                ones += int((p == 1.0).sum())
+                l = fp32(l.astype(np.float64) * c + p.astype(np.float64).sum(axis=1))
+                prod = p.astype(np.float64) @ v[b, kv, j0: j0 + block]
+                if accumulate == "bf16":
+                    u = bf16_rne(fp32(prod))
+                    scaled = bf16_rne(fp32(obar.astype(np.float64) * c[:, None]))
+                    obar = bf16_rne(fp32(scaled.astype(np.float64) + u.astype(np.float64)))
+                else:
+                    obar = fp32(obar.astype(np.float64) * c[:, None] + prod)
                 m_prev = m
             with np.errstate(divide="ignore", invalid="ignore"):
                 o[b, h] = bf16_rne(fp32(obar.astype(np.float64) / l.astype(np.float64)[:, None]))
                 lse[b, h] = fp32(fp32(m_prev) + fp32(np.log(l.astype(np.float64))))
             obar_all[b, h] = obar
-    return {"o": o, "lse": lse, "obar": obar_all}
+    return {"o": o, "lse": lse, "obar": obar_all, "operational_ones": ones}

@@ -19,6 +19,8 @@ _LIB = None
 PFA_OK = 0
 # pfa_attn_fwd_ex flags and the monitor's size (include/pfa.h)
 FWD_UNFUSED_BF16_PV = 1
+FWD_PBAR_E4M3 = 2
+FWD_PBAR_MXFP4 = 4
 TIE_BINS = 8
 MONITOR_WORDS = 1 + TIE_BINS
 # pfa_attn_bwd_ex flags (include/pfa.h)

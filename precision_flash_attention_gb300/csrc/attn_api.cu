@@ -223,9 +223,12 @@ int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa
   if (!q || !k || !v || !o || !lse) return PFA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H_q, H_kv, N, d);
   if (rc != PFA_OK) return rc;
-  if (flags & ~static_cast<unsigned>(PFA_FWD_UNFUSED_BF16_PV)) return PFA_ERR_INVALID_ARG;
+  if (flags & ~static_cast<unsigned>(PFA_FWD_UNFUSED_BF16_PV | PFA_FWD_PBAR_E4M3 | PFA_FWD_PBAR_MXFP4))
+    return PFA_ERR_INVALID_ARG;
+  if ((flags & PFA_FWD_PBAR_E4M3) && (flags & PFA_FWD_PBAR_MXFP4)) return PFA_ERR_INVALID_ARG;
   const bool profile = (flags & PFA_FWD_UNFUSED_BF16_PV) != 0;
-  if (profile && d != 64) return PFA_ERR_UNSUPPORTED;
+  const int pbar = (flags & PFA_FWD_PBAR_E4M3) ? 1 : (flags & PFA_FWD_PBAR_MXFP4) ? 2 : 0;
+  if ((profile || pbar) && d != 64) return PFA_ERR_UNSUPPORTED;
   if (!good_scale(scale) || fix_mode < 0 || fix_mode > 2) return PFA_ERR_INVALID_ARG;
   if (fix_mode == 1 && !(std::isfinite(beta) && beta > 1.f)) return PFA_ERR_INVALID_ARG;
   const bool ties = fix_mode != 0 || counters != nullptr || monitor != nullptr;
@@ -253,7 +256,9 @@ int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa
   a.eps_raw = ties ? eps / scale : 0.f;
   a.tau_raw = static_cast<float>(kRoundToOneWindow / scale);
   a.profile = profile ? 1 : 0;
+  a.pbar = pbar;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pbar) return launched(pfa::launch_fwd_lowp(tq, tk, tv, a, st));
   if (profile || monitor) return launched(pfa::launch_fwd_study(tq, tk, tv, a, st));
   return launched(pfa::launch_fwd(tq, tk, tv, a, st));
 }
@@ -367,6 +372,23 @@ int bwd_launch(const BwdLaunch& L, cudaStream_t st) {
   return launched(pfa::launch_bwd(L.tq, L.tk, L.tv, L.tdo, L.tdq, L.tdk, L.tdv, L.a, st));
 }
 
+// dK, dV from the key-outer kernel without its dQ product (L prepared with no dQ
+// workspace), then dQ = alpha dS K from the query-outer pass (split: dS as BF16 hi + lo).
+int bwd_query_outer(const BwdLaunch& L, pfa_bf16* dq, const float* lse, const float* delta, bool split,
+                    cudaStream_t st) {
+  pfa::DqArgs da;
+  da.s = L.a.s;
+  da.lse = lse;
+  da.delta = delta;
+  da.dq = dq;
+  da.err = L.a.err;
+  da.err_site = L.a.err_site;
+  da.split = split ? 1 : 0;
+  const int rc = bwd_launch(L, st);
+  if (rc != PFA_OK) return rc;
+  return launched(pfa::launch_dq(L.tq, L.tk, L.tv, L.tdo, da, st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -380,10 +402,14 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   if (rc != PFA_OK) return rc;
   if (!aligned16(dq)) return PFA_ERR_MISALIGNED;
   BwdLaunch L;
-  if ((rc = bwd_prepare(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, causal, scale,
-                        &L)) != PFA_OK)
+  if ((rc = bwd_prepare(q, k, v, dO, lse, delta, d == 128 ? nullptr : dq_accum, dk, dv, B, H_q, H_kv,
+                        N, d, causal, scale, &L)) != PFA_OK)
     return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // At d = 128 the key-outer kernel has no shared memory left to stage dQ for a tensor
+  // reduce and would add it with vector atomics; the query-outer pass is faster there
+  // (and deterministic), so it computes dQ and the workspace is not used.
+  if (d == 128) return bwd_query_outer(L, dq, lse, delta, /*split=*/false, st);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
   if ((rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
     return rc;
@@ -421,17 +447,8 @@ int pfa_attn_bwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, con
   if ((rc = bwd_prepare(q, k, v, dO, lse, delta, nullptr, dk, dv, B, H_q, H_kv, N, d, causal, scale,
                         &L)) != PFA_OK)
     return rc;
-  pfa::DqArgs da;
-  da.s = L.a.s;
-  da.lse = lse;
-  da.delta = delta;
-  da.dq = dq;
-  da.err = L.a.err;
-  da.err_site = L.a.err_site;
-  da.split = (flags & PFA_BWD_DQ_SPLIT) ? 1 : 0;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if ((rc = bwd_launch(L, st)) != PFA_OK) return rc;
-  return launched(pfa::launch_dq(L.tq, L.tk, L.tv, L.tdo, da, st));
+  return bwd_query_outer(L, dq, lse, delta, (flags & PFA_BWD_DQ_SPLIT) != 0,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* pfa_status_string(int status) {

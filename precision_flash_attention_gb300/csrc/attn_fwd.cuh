@@ -38,8 +38,13 @@
 // histogram of tie multiplicities), PROFILE (d = 64 only: each key tile's product
 // Pbar V is rounded to BF16 and accumulated across tiles in BF16, as an
 // implementation that stores the unnormalised product in BF16 does; a study
-// variant, not the fused path). The instantiations live in attn_fwd.cu (the
-// fused path) and attn_fwd_study.cu (monitor and profile).
+// variant, not the fused path), PBAR (the format of the Pbar operand: BF16, or,
+// for the study of narrower formats, FP8 E4M3 or MXFP4 = E2M1 with one
+// power-of-two scale per 32 keys; the rounded values are exact in BF16, so the
+// BF16 product with FP32 accumulation computes what a product in that format
+// with FP32 accumulation does, and l sums the rounded values). The instantiations
+// live in attn_fwd.cu (the fused path), attn_fwd_study.cu (monitor and profile)
+// and attn_fwd_lowp.cu (the narrow Pbar formats).
 #pragma once
 
 #include "pfa_device.cuh"
@@ -66,6 +71,8 @@ constexpr float kEpsShift = 0.03125f;  // 2^-5
 // Smallest FP32 value that rounds to BF16 1.0 (the midpoint 1 - 2^-9 ties to 1.0).
 constexpr float kBf16OneThreshold = 0.998046875f;
 constexpr int kTieBins = 8;            // tie multiplicity 1..7 and >= 8
+// Formats of the Pbar operand of the Pbar V product.
+constexpr int kPbarBf16 = 0, kPbarE4m3 = 1, kPbarMxfp4 = 2;
 
 template <int D, bool PROFILE>
 struct FwdLayout {
@@ -103,7 +110,7 @@ struct FwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE>
+template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE, int PBAR = kPbarBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
@@ -505,15 +512,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // distinct entries differ in their block or in their class. The block
         // count is known with the maximum, and only warps where some row jumps
         // count it. Only warps where some row's new maximum is alone in its block
-        // gather the class maxima, after the exponentials: such a row is taken as
-        // single first, and if the class maxima show a second entry the tile is
-        // recomputed under the repeated shift (taken only when a tie sits inside
-        // one block of a new maximum).
+        // take the class maxima, before the exponentials, so every tile is
+        // exponentiated once, under its final shift, and the scores can die as
+        // the exponentials consume them.
         bool jump = false;
         int nb = 0;
         float thr_eps = 0.f;
         bool rep_use = rep;
-        bool need_cls = false;
         if (kTies) {
           thr_eps = t1 - args.eps_raw;
           jump = t1 > m1 && m1 < thr_eps;
@@ -526,7 +531,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (t1 >= m1 - args.eps_raw && t1 > -INFINITY) {
             rep_use = true;
           }
-          need_cls = __any_sync(0xFFFFFFFFu, jump && nb < 2);
+          if (__any_sync(0xFFFFFFFFu, jump && nb < 2)) {
+            // Class maxima (column mod 16) over the whole tile.
+            int ne = 0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              auto x = [&](int k) { return __uint_as_float(v[16 * k + e]); };
+              const float c = fmax3(fmax3(x(0), x(1), x(2)), fmax3(x(3), x(4), x(5)), fmaxf(x(6), x(7)));
+              ne += c >= thr_eps ? 1 : 0;
+            }
+            if (jump && nb < 2 && ne >= 2) rep_use = true;
+          }
         }
         const float m1_old = m1;
         m1 = fmaxf(m1, t1);
@@ -534,23 +549,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Pbar = exp(S - m) in FP32; l sums it (the profile sums its BF16 cast); the
         // BF16 casts go to TMEM.
-        const float l0s = l0, l1s = l1;
-        float m_new = m_sh, corr = 1.f;
-        bool changed = false;
+        const float m_new = shift_of(m1, rep_use);
+        const bool changed = (j > 0) && (m_new != m_sh);
+        const float corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
+        l0 *= corr;
+        l1 *= corr;
         int cnt_tile = 0, eps_tile = 0, ones_tile = 0;
-        auto exp_pass = [&](bool first) {
-          m_new = shift_of(m1, rep_use);
-          changed = (j > 0) && (m_new != m_sh);
-          corr = changed ? ex2_approx((m_sh - m_new) * kLog2e) : 1.f;
-          l0 = l0s * corr;
-          l1 = l1s * corr;
+        {
           const float nml2 = -m_new * kLog2e;
           const float thr = m1 - args.tau_raw;
           const float thr_e = m1 - args.eps_raw;
-          cnt_tile = eps_tile = ones_tile = 0;
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             uint32_t pk[32];
+            // Pbar pair u (FP32) into the BF16 operand, the row sum and the monitor. With
+            // a narrow Pbar format the pair arrives already rounded to it (its values are
+            // exact in BF16) and l sums those values, the weights the product uses.
+            auto finish = [&](int u, float p0, float p1) {
+              pk[u] = pack_bf16x2(p0, p1);
+              if constexpr (PBAR != kPbarBf16) {
+                add2(l0, l1, p0, p1);
+                if (kMonitor) ones_tile += (p0 == 1.f) + (p1 == 1.f);
+              } else {
+                if constexpr (PROFILE) {
+                  // The profile normalises by the weights its product uses: BF16 Pbar.
+                  add2(l0, l1, bf16lo_to_f32(pk[u]), bf16hi_to_f32(pk[u]));
+                } else {
+                  add2(l0, l1, p0, p1);
+                }
+                // BF16(Pbar) == 1 exactly when Pbar >= 1 - 2^-9 (Pbar <= 1 here).
+                if (kMonitor) ones_tile += (p0 >= kBf16OneThreshold) + (p1 >= kBf16OneThreshold);
+              }
+            };
+            [[maybe_unused]] float pm[PBAR == kPbarMxfp4 ? 64 : 1];
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
               const float x0 = __uint_as_float(v[64 * half + 2 * u]);
@@ -558,17 +589,47 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (kCount) cnt_tile += (x0 >= thr) + (x1 >= thr);
               if (kMonitor) eps_tile += (x0 >= thr_e) + (x1 >= thr_e);
               float y0, y1;
-              fma2(y0, y1, x0, x1, sl2, nml2);
-              const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-              pk[u] = pack_bf16x2(p0, p1);
-              if constexpr (PROFILE) {
-                // The profile normalises by the weights its product uses: BF16 Pbar.
-                add2(l0, l1, bf16lo_to_f32(pk[u]), bf16hi_to_f32(pk[u]));
+              if constexpr (PBAR != kPbarBf16) {
+                // The exponent as (alpha x - m) log2 e, so that it is exactly 0 where the score
+                // is the shift: a narrow format's rounding (and MXFP4's power-of-two scale)
+                // turns on whether Pbar is 1 or just below it.
+                // Rounded operations that are never contracted into an FMA.
+                y0 = __fmul_rn(__fsub_rn(__fmul_rn(x0, alpha), m_new), kLog2e);
+                y1 = __fmul_rn(__fsub_rn(__fmul_rn(x1, alpha), m_new), kLog2e);
               } else {
-                add2(l0, l1, p0, p1);
+                fma2(y0, y1, x0, x1, sl2, nml2);
               }
-              // BF16(Pbar) == 1 exactly when Pbar >= 1 - 2^-9 (Pbar <= 1 here).
-              if (kMonitor) ones_tile += (p0 >= kBf16OneThreshold) + (p1 >= kBf16OneThreshold);
+              float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+              if constexpr (PBAR == kPbarMxfp4) {
+                pm[2 * u] = p0;
+                pm[2 * u + 1] = p1;
+              } else {
+                if constexpr (PBAR == kPbarE4m3) e4m3_round2(p0, p1);
+                finish(u, p0, p1);
+              }
+            }
+            if constexpr (PBAR == kPbarMxfp4) {
+              // MXFP4: 32 consecutive keys share the scale X = 2^(floor(log2 amax) - 2);
+              // each Pbar becomes X E2M1(Pbar / X), saturating at 6 X.
+#pragma unroll
+              for (int blk = 0; blk < 2; ++blk) {
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) amax = fmax3(amax, pm[32 * blk + e], pm[32 * blk + e + 1]);
+                const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                  float a = 0.f, b = 0.f;
+                  if (amax > 0.f) {
+                    a = ldexpf(pm[32 * blk + e], 2 - ex);
+                    b = ldexpf(pm[32 * blk + e + 1], 2 - ex);
+                    e2m1_round2(a, b);
+                    a = ldexpf(a, ex - 2);
+                    b = ldexpf(b, ex - 2);
+                  }
+                  finish(16 * blk + e / 2, a, b);
+                }
+              }
             }
             if constexpr (L::kSplitP) {
               // Obar_t and the Pbar_t columns are free once the previous key
@@ -576,30 +637,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               // waited for the last product of the previous item). Without split
               // Pbar, S_t of this tile was committed after that product.
               // A failed wait ends the loop at the bottom of this iteration.
-              if (first && half == 0 && j > 0) {
+              if (half == 0 && j > 0) {
                 ok = wait_warp(bar(L::bPVDone + t), (ct + j - 1) & 1, ctl);
                 tc_fence_after();
               }
             }
             tmem_st32(tP + 32 * half, pk);
-          }
-        };
-        exp_pass(true);
-        if (kTies && need_cls) {
-          // Class maxima (column mod 16) over the whole tile.
-          int ne = 0;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            auto x = [&](int k) { return __uint_as_float(v[16 * k + e]); };
-            const float c = fmax3(fmax3(x(0), x(1), x(2)), fmax3(x(3), x(4), x(5)), fmaxf(x(6), x(7)));
-            ne += c >= thr_eps ? 1 : 0;
-          }
-          const bool wrong = jump && nb < 2 && ne >= 2;
-          if (wrong) rep_use = true;
-          // Mode 0 keeps the flag for the counters only: its shift does not move.
-          if (MODE != 0 && __any_sync(0xFFFFFFFFu, wrong)) {
-            tmem_st_wait();   // the second pass stores over the first one's Pbar
-            exp_pass(false);
           }
         }
         rep = rep_use;
@@ -734,11 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE>
+template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE, int PBAR = kPbarBf16>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D, PROFILE>;
-  auto kern = attn_fwd_kernel<D, MODE, CAUSAL, MON, PROFILE>;
+  auto kern = attn_fwd_kernel<D, MODE, CAUSAL, MON, PROFILE, PBAR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   // Persistent: one CTA per SM (at most one per work item).

@@ -100,6 +100,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
+// The FP32 pair (a, b) rounded to the nearest FP8 E4M3 values (ties to even,
+// saturating at 448), returned as FP32 (exact: E4M3 values are FP16 values).
+__device__ __forceinline__ void e4m3_round2(float& a, float& b) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 t;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"   // upper byte from the first source
+      "cvt.rn.f16x2.e4m3x2 %0, t;\n\t}"               // lower byte to the lower half
+      : "=r"(h)
+      : "f"(b), "f"(a));
+  a = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  b = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+}
+// The FP32 pair (a, b) rounded to the nearest FP4 E2M1 values (0, 0.5, 1, 1.5, 2,
+// 3, 4, 6; ties to even, saturating at 6), returned as FP32.
+__device__ __forceinline__ void e2m1_round2(float& a, float& b) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"   // upper nibble from the first source
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"               // lower nibble to the lower half
+      : "=r"(h)
+      : "f"(b), "f"(a));
+  a = __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+  b = __half2float(__ushort_as_half(static_cast<unsigned short>(h >> 16)));
+}
+
 // x rounded to the nearest BF16 value (ties to even), returned as FP32.
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t p) { return __uint_as_float(p << 16); }

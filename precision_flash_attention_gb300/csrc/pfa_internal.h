@@ -61,6 +61,7 @@ struct FwdArgs {
   float eps_raw;           // tie tolerance in units of the unscaled score Q.K
   float tau_raw;           // BF16 round-to-one window in units of Q.K
   int profile;             // the unfused BF16 Pbar V study profile (d = 64)
+  int pbar;                // the Pbar operand's format: 0 BF16, 1 FP8 E4M3, 2 MXFP4 (d = 64)
 };
 
 struct DeltaAltArgs {
@@ -99,6 +100,9 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // BF16 profile (a.profile, d = 64); counters as in launch_fwd.
 cudaError_t launch_fwd_study(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const FwdArgs& a, cudaStream_t stream);
+// The narrow Pbar formats (a.pbar 1 or 2; d = 64, monitor counted, profile or fused).
+cudaError_t launch_fwd_lowp(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long rows, int d,
                          cudaStream_t stream);
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -178,10 +178,12 @@ def test_fwd_ex_validates(lib):
         a.update(kw)
         return lib.pfa_attn_fwd_ex(*a.values())
 
-    assert call(flags=2) == inv                       # an unknown flag bit
+    assert call(flags=8) == inv                       # an unknown flag bit
+    assert call(flags=2 | 4) == inv                   # both narrow Pbar formats at once
     assert call(monitor=A + 4) == mis                 # the monitor must be 8-byte aligned
     assert call(monitor=A, eps=-1.0) == inv           # the monitor needs a valid eps
     assert call(q=None) == inv
     if _no_device():
-        assert call(flags=1, d=128) == -3             # the unfused profile is d = 64 only
-        assert call(flags=1) not in (inv, mis)
+        for fl in (1, 2, 4, 1 | 2):
+            assert call(flags=fl, d=128) == -3        # the study variants are d = 64 only
+            assert call(flags=fl) not in (inv, mis)

@@ -175,3 +175,63 @@ def test_monitor_histogram_agrees_with_the_counters(causal):
             # Mode 0 never moves a shift away from the running maximum: every exact one of the
             # final shift was handed to the product in its own tile too.
             assert r["operational_ones"] >= f["counters"]["ones"]
+
+
+# ---------------------------------------------------------------- narrower Pbar formats
+def _tied_row(r_m):
+    # Row 0 of a 4-key block: keys 0 and 1 score r_m (a repeated maximum), keys 2 and 3 far
+    # below (-30); the other rows are copies. Scale 1.
+    q = np.ones((1, 1, 4, 1))
+    k = np.zeros((1, 1, 4, 1))
+    k[0, 0, :, 0] = [r_m, r_m, -30.0, -30.0]
+    v = np.ones((1, 1, 4, 1))
+    return q, k, v
+
+
+def test_e4m3_pbar_worked_cases():
+    # Mode 2 subtracts 2^-5 on a repeated maximum: exp(-2^-5) = 0.9692 lies above the E4M3
+    # midpoint 1 - 2^-5 between 0.9375 and 1, so Pbar rounds back to exactly 1 (two per row).
+    q, k, v = _tied_row(1.0)
+    r = oracle.attn_fwd_blockwise(q, k, v, scale=1.0, fix_mode=2, block=4, pbar="e4m3", accumulate="fp32")
+    assert r["operational_ones"] == 2 * 4
+    # Mode 1 with beta = 2 on a repeated maximum of 16: Pbar = e^-16 = 1.1e-7 lies below half
+    # the smallest E4M3 subnormal (2^-10), so every weight is 0 and l = 0 (NaN output).
+    q, k, v = _tied_row(16.0)
+    r = oracle.attn_fwd_blockwise(q, k, v, scale=1.0, fix_mode=1, block=4, pbar="e4m3", accumulate="fp32")
+    assert r["operational_ones"] == 0 and np.isnan(r["o"]).all()
+    # In BF16 the same two cases keep every Pbar below 1 and finite.
+    for mode, rm in ((2, 1.0), (1, 16.0)):
+        q, k, v = _tied_row(rm)
+        r = oracle.attn_fwd_blockwise(q, k, v, scale=1.0, fix_mode=mode, block=4, pbar="bf16",
+                                      accumulate="fp32")
+        assert r["operational_ones"] == 0 and np.isfinite(r["o"]).all()
+
+
+def test_mxfp4_pbar_worked_case():
+    # Mode 2 on a repeated maximum: both tied weights are 0.9692, the block's largest; the scale
+    # is 2^(floor(log2 0.9692) - 2) = 1/8 and 0.9692 / (1/8) = 7.75 saturates at 6: Pbar = 0.75.
+    # The far keys (e^-31) are below the smallest E2M1 step at that scale and become 0, so O is
+    # V's mean over the two tied keys exactly, and no Pbar equals 1.
+    q, k, v = _tied_row(1.0)
+    v[0, 0, :, 0] = [2.0, 4.0, 100.0, 100.0]
+    r = oracle.attn_fwd_blockwise(q, k, v, scale=1.0, fix_mode=2, block=4, pbar="mxfp4", accumulate="fp32")
+    assert r["operational_ones"] == 0
+    assert np.all(r["o"][0, 0, :, 0] == 3.0)
+    assert np.all(r["obar"][0, 0, :, 0] == 0.75 * 6.0)
+
+
+@pytest.mark.parametrize("pbar", ["e4m3", "mxfp4"])
+@pytest.mark.parametrize("accumulate", ["bf16", "fp32"])
+def test_blockwise_without_roundings_is_the_float64_pass(monkeypatch, pbar, accumulate):
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 2, 70, 8))
+    k = rng.standard_normal((1, 1, 70, 8))
+    v = rng.standard_normal((1, 1, 70, 8))
+    k[0, 0, 9] = k[0, 0, 4]
+    ref = oracle.attn_fwd(q, k, v, causal=True, scale=0.375)
+    for name in ("fp32", "bf16_rne", "ftz32", "e4m3_rne", "mx_e2m1"):
+        monkeypatch.setattr(oatt, name, lambda x, *a, **kw: np.asarray(x, dtype=np.float64))
+    for mode in (0, 1, 2):
+        r = oracle.attn_fwd_blockwise(q, k, v, causal=True, scale=0.375, fix_mode=mode, block=32,
+                                      pbar=pbar, accumulate=accumulate)
+        np.testing.assert_allclose(r["o"], ref["o"], rtol=0, atol=1e-12)

@@ -146,5 +146,53 @@ def test_unfused_profile_rejects_d128_and_unknown_flags():
     with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):
         pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=1)
     with pytest.raises(pfa.PfaError, match="INVALID_ARG"):
+        pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=8)
+    with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):
         pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=2)
     assert pfa.device_error() == 0
+
+
+# ---------------------------------------------------------------- narrower Pbar formats
+@pytest.mark.parametrize("profile", [False, True], ids=["fused", "unfused"])
+@pytest.mark.parametrize("pbar", ["e4m3", "mxfp4"])
+@pytest.mark.parametrize("shape", [(1, 2, 1, 300, 64, True), (1, 2, 2, 257, 64, False),
+                                   (2, 2, 1, 700, 64, True)], ids=lambda s: "x".join(map(str, s)))
+def test_narrow_pbar_matches_oracle(shape, pbar, profile):
+    # Pbar rounded to FP8 E4M3 or MXFP4 before the product, Obar in FP32 (fused) or in BF16 per
+    # key tile (the unfused profile), against the oracle's blockwise pass over 128-key blocks.
+    B, Hq, Hkv, N, d, causal = shape
+    t = inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.7, std_do=1.0, seed=N + len(pbar))
+    for mode in (0, 1, 2):
+        kw = dict(causal=causal, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
+        got = _fwd(t, unfused_bf16_pv=profile, pbar=pbar, **kw)
+        q, k, v = (f64(t[n]) for n in ("q", "k", "v"))
+        ref = oracle.attn_fwd_blockwise(q, k, v, block=128, pbar=pbar,
+                                        accumulate="bf16" if profile else "fp32", **kw)
+        assert_fwd_close({"o": f64(got["o"]), "lse": f64(got["lse"])}, ref, f"{pbar} {shape} {mode}")
+        assert got["operational_ones"] == ref["operational_ones"]
+
+
+@pytest.mark.parametrize("pbar", ["e4m3", "mxfp4"])
+def test_narrow_pbar_on_tied_maxima(pbar):
+    # The tie probe (a sink key repeated twice, logit 16): in E4M3 mode 2's shift exp(-2^-5)
+    # rounds back to exactly 1, so the product sees as many ones as without the fix, and mode
+    # 1's beta shift (e^-16) falls below E4M3's range, leaving l = 0; MXFP4's block scale keeps
+    # mode 1 finite and saturates mode 2's 0.969 to 0.75. The GPU counts and NaN rows match the
+    # oracle's.
+    t = inputs.tie_probe(1, 2, 512, 64, ties=2, seed=4)
+    q, k, v = (f64(t[n]) for n in ("q", "k", "v"))
+    res = {}
+    for mode in (0, 1, 2):
+        kw = dict(causal=True, scale=0.125, fix_mode=mode, beta=2.0, eps=1e-3)
+        got = _fwd(t, pbar=pbar, **kw)
+        ref = oracle.attn_fwd_blockwise(q, k, v, block=128, pbar=pbar, accumulate="fp32", **kw)
+        nan_g = np.isnan(f64(got["o"])).any(axis=-1)
+        nan_r = np.isnan(ref["o"]).any(axis=-1)
+        assert np.array_equal(nan_g, nan_r)
+        assert got["operational_ones"] == ref["operational_ones"]
+        res[mode] = (got["operational_ones"], int(nan_g.sum()))
+    print(f"{pbar}: operational ones / NaN rows per mode {res}")
+    if pbar == "e4m3":
+        assert res[2][0] == res[0][0] > 0 and res[1][1] > 0.9 * 2 * 512
+    else:
+        assert res[2][0] < res[0][0] and res[1][1] == 0
