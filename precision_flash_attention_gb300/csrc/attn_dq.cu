@@ -14,17 +14,19 @@
 //
 // CTA = one (batch, query head, 128-row query tile), heaviest causal tiles first.
 // 320 threads: warp 0 TMA producer, warp 1 TMEM owner and MMA issuer, warps 2..9
-// compute. Compute warp w handles TMEM lane quarter w % 4 (32 query rows) and key
-// columns [64 h, 64 h + 64) with h = (w - 2) / 4, so each SM sub-partition runs
-// two compute warps.
-// TMEM: S = Q K_j^T in [0, 128), dP = dO V_j^T in [128, 256), dQ in [256, 256 + d).
-// dS (BF16, two keys per 32-bit column) is written over the S columns the warp
-// has already read: keys 32 c .. 32 c + 31 of S occupy columns [32 c, 32 c + 32),
-// and their dS hi goes to [32 c, 32 c + 16), lo to [32 c + 16, 32 c + 32). Key
-// step kk (16 keys) of the dQ product therefore reads hi at 32 (kk / 2) + 8 (kk % 2).
-// Tensor-core order per key tile j: dQ(j - 1) (it reads dS(j - 1) from the S
-// columns), then S(j) and dP(j); in-order execution keeps S(j) from overwriting
-// dS(j - 1) before dQ(j - 1) has read it.
+// compute. Each 128-key tile is processed as two 64-key halves u = 2 j, 2 j + 1,
+// in two TMEM buffers b = u % 2 at [128 b, 128 b + 128): S_u = Q K_u^T in the
+// first 64 columns, dP_u = dO V_u^T in the next 64; dQ sits in [256, 256 + d).
+// Compute warp w handles TMEM lane quarter w % 4 (32 query rows) and the 32 keys
+// [32 c, 32 c + 32) of each half, c = (w - 2) / 4, so each SM sub-partition runs
+// two compute warps. dS (BF16, two keys per 32-bit column) is written over the S
+// columns the warp has read: its 32 keys occupy [32 c, 32 c + 32) of the half's
+// S, hi in the first 16 columns and lo in the next 16, so key step kk (16 keys) of
+// the dQ product reads hi at 32 (kk / 2) + 8 (kk % 2).
+// Tensor-core order: S_0, dP_0, S_1, dP_1, then per half u: dQ_u, S_(u+2), dP_(u+2).
+// The compute warps form dS_(u+1) while the tensor core runs dQ_u and S_(u+2),
+// and in-order execution keeps S_(u+2) (same buffer) from overwriting dS_u before
+// dQ_u has read it.
 #include "pfa_device.cuh"
 
 namespace pfa {
@@ -32,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kHalf = kTile / 2;   // keys of one half-tile
 
 template <int D>
 struct DqLayout {
@@ -46,20 +49,21 @@ struct DqLayout {
   static constexpr int bQFull = 0;
   static constexpr int bKVFull = 1;                     // + stage
   static constexpr int bKVEmpty = bKVFull + kStages;    // + stage
-  static constexpr int bSFull = bKVEmpty + kStages;     // S(j) and dP(j) are in TMEM
-  static constexpr int bDSReady = bSFull + 1;           // the compute warps wrote dS(j)
-  static constexpr int bDQDone = bDSReady + 1;          // the last dQ product completed
+  static constexpr int bSFull = bKVEmpty + kStages;     // + buffer: S_u and dP_u are in TMEM
+  static constexpr int bDSReady = bSFull + 2;           // + buffer: the compute warps wrote dS_u
+  static constexpr int bDQDone = bDSReady + 2;          // the last dQ product completed
   static constexpr int bDrain = bDQDone + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kTmemSlot = kBars + kNumBars * 8;
   static constexpr int kAbort = kTmemSlot + 4;
   static constexpr int kBytes = kAbort + 4;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+  static constexpr uint32_t kColDQ = 256;
   static_assert(kColDQ + D <= 512, "TMEM columns");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-// Column of the BF16 dS hi values of key step kk (16 keys); lo sits 16 columns on.
+// Column of the BF16 dS hi values of key step kk (16 keys) within a half's S
+// columns; lo sits 16 columns on.
 __device__ __forceinline__ uint32_t ds_col(int kk) {
   return 32u * static_cast<uint32_t>(kk >> 1) + 8u * static_cast<uint32_t>(kk & 1);
 }
@@ -85,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = bh % sh.Hq;
   const int bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
   const int n_kt = CAUSAL ? min(qt + 1, n_t) : n_t;
+  const int n_u = 2 * n_kt;   // half-tiles
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -99,8 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(L::bKVFull + s), 1);
       mbar_init(bar(L::bKVEmpty + s), 1);
     }
-    mbar_init(bar(L::bSFull), 1);
-    mbar_init(bar(L::bDSReady), 8);
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(bar(L::bSFull + u), 1);
+      mbar_init(bar(L::bDSReady + u), 8);
+    }
     mbar_init(bar(L::bDQDone), 1);
     mbar_init(bar(L::bDrain), 1);
     fence_mbar_init();
@@ -145,60 +152,78 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_drain(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
     } else if (warp == 1) {
       // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-      constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S, dP
-      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ: A = dS in TMEM, B = K MN-major
-      // dQ(j) += dS(j) K_j from stage s: hi, then lo into the same accumulator.
-      auto issue_dq = [&](int j, int s) {
-        const uint32_t sK = sbase + L::kK + s * L::kTileBytes;
+      constexpr uint32_t idS = idesc_bf16(128, kHalf, false, false);  // S_u, dP_u: N = 64 keys
+      constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);      // dQ: A = dS in TMEM, B = K MN-major
+      // S_u = Q K_u^T and dP_u = dO V_u^T into buffer u % 2; K_u, V_u are rows
+      // [64 (u % 2), 64 (u % 2) + 64) of the key tile in stage (u / 2) % 2.
+      auto issue_sdp = [&](int u) {
+        const uint32_t tb = tmem + 128u * static_cast<uint32_t>(u & 1);
+        const int s = (u >> 1) % L::kStages;
+        const uint32_t hoff = static_cast<uint32_t>(u & 1) * kHalf * 128;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_tmem_a_warp(tmem + L::kColDQ, tmem + L::kColS + ds_col(kk),
-                                sdesc_sw128(sK + kk * 2048, L::kPanelBytes, 1024), idDQ,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          umma_bf16_warp(tb, sdesc_sw128(sbase + L::kQ + koff, 16, 1024),
+                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + hoff + koff, 16, 1024), idS, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          umma_bf16_warp(tb + kHalf, sdesc_sw128(sbase + L::kDO + koff, 16, 1024),
+                         sdesc_sw128(sbase + L::kV + s * L::kTileBytes + hoff + koff, 16, 1024), idS, kk > 0);
+        }
+        umma_commit_warp(bar(L::bSFull + (u & 1)));
+      };
+      // dQ += dS_u K_u: hi, then lo into the same accumulator.
+      auto issue_dq = [&](int u) {
+        const uint32_t tb = tmem + 128u * static_cast<uint32_t>(u & 1);
+        const int s = (u >> 1) % L::kStages;
+        const uint32_t sK = sbase + L::kK + s * L::kTileBytes;
+        const int h4 = 4 * (u & 1);   // the half's first key step within the tile
+#pragma unroll
+        for (int kk = 0; kk < kHalf / 16; ++kk)
+          umma_bf16_tmem_a_warp(tmem + L::kColDQ, tb + ds_col(kk),
+                                sdesc_sw128(sK + (h4 + kk) * 2048, L::kPanelBytes, 1024), idDQ,
+                                (u > 0 || kk > 0) ? 1u : 0u);
         if constexpr (SPLIT) {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            umma_bf16_tmem_a_warp(tmem + L::kColDQ, tmem + L::kColS + ds_col(kk) + 16u,
-                                  sdesc_sw128(sK + kk * 2048, L::kPanelBytes, 1024), idDQ, 1u);
+          for (int kk = 0; kk < kHalf / 16; ++kk)
+            umma_bf16_tmem_a_warp(tmem + L::kColDQ, tb + ds_col(kk) + 16u,
+                                  sdesc_sw128(sK + (h4 + kk) * 2048, L::kPanelBytes, 1024), idDQ, 1u);
         }
-        umma_commit_warp(bar(L::bKVEmpty + s));   // the last reader of K_j, V_j
+        // The second half's product is the last reader of the tile's K and V.
+        if (u & 1) umma_commit_warp(bar(L::bKVEmpty + s));
+      };
+      // Half u needs its key tile (u / 2) in shared memory; the first half waits.
+      auto tile_ready = [&](int u) {
+        if (u & 1) return true;
+        const int j = u >> 1;
+        return wait_warp(bar(L::bKVFull + j % L::kStages), (j / L::kStages) & 1, ctl);
       };
       bool ok = wait_warp(bar(L::bQFull), 0, ctl);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % L::kStages;
-        if (!(ok = wait_warp(bar(L::bKVFull + s), (j / L::kStages) & 1, ctl))) break;
-        if (j > 0) {
-          if (!(ok = wait_warp(bar(L::bDSReady), (j - 1) & 1, ctl))) break;
+      for (int u = 0; ok && u < 2; ++u) {
+        if (!(ok = tile_ready(u))) break;
+        tc_fence_after();
+        issue_sdp(u);
+      }
+      for (int u = 0; ok && u < n_u; ++u) {
+        if (!(ok = wait_warp(bar(L::bDSReady + (u & 1)), (u >> 1) & 1, ctl))) break;
+        tc_fence_after();
+        issue_dq(u);
+        if (u + 2 < n_u) {
+          if (!(ok = tile_ready(u + 2))) break;
           tc_fence_after();
-          issue_dq(j - 1, (j - 1) % L::kStages);
+          issue_sdp(u + 2);
         }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          umma_bf16_warp(tmem + L::kColS, sdesc_sw128(sbase + L::kQ + koff, 16, 1024),
-                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idKK, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          umma_bf16_warp(tmem + L::kColDP, sdesc_sw128(sbase + L::kDO + koff, 16, 1024),
-                         sdesc_sw128(sbase + L::kV + s * L::kTileBytes + koff, 16, 1024), idKK, kk > 0);
-        }
-        umma_commit_warp(bar(L::bSFull));
       }
-      if (ok && (ok = wait_warp(bar(L::bDSReady), (n_kt - 1) & 1, ctl))) {
-        tc_fence_after();
-        issue_dq(n_kt - 1, (n_kt - 1) % L::kStages);
-        umma_commit_warp(bar(L::bDQDone));
-      }
+      if (ok) umma_commit_warp(bar(L::bDQDone));
       // No MMA may still read shared memory or write TMEM at teardown.
       umma_commit_warp(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, ctl);
     } else {
       // ---------------- compute warps ----------------
       const uint32_t quarter = warp & 3;
-      const int half = (warp - 2) >> 2;          // key columns [64 half, 64 half + 64)
+      const int c = (warp - 2) >> 2;             // keys [32 c, 32 c + 32) of each half
       const int r = quarter * 32 + lane;         // query row within the tile == TMEM lane
       const int qrow = q0 + r;
       const uint32_t lane_off = (quarter * 32u) << 16;
@@ -209,68 +234,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ndelta = row_ok ? -args.delta[rowi] : 0.f;
       const float sl2 = sh.scale_log2;
       bool ok = true;
-      for (int j = 0; j < n_kt; ++j) {
-        const int k0 = j * kTile;
-        const bool need_mask = (CAUSAL && k0 + kTile > q0) || (k0 + kTile > N);
-        if (!(ok = wait_warp(bar(L::bSFull), j & 1, ctl))) break;
+      for (int u = 0; u < n_u; ++u) {
+        const int k0 = (u >> 1) * kTile + (u & 1) * kHalf + 32 * c;   // this warp's first key
+        const bool need_mask = (CAUSAL && k0 + 32 > q0) || (k0 + 32 > N);
+        const uint32_t tb = tmem + 128u * static_cast<uint32_t>(u & 1) + lane_off + 32u * c;
+        if (!(ok = wait_warp(bar(L::bSFull + (u & 1)), (u >> 1) & 1, ctl))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          const int kc = 64 * half + 32 * c;   // first key column of this chunk
-          uint32_t sv[32], pv[32];
-          tmem_ld32(tmem + L::kColS + lane_off + kc, sv);
-          tmem_ld32(tmem + L::kColDP + lane_off + kc, pv);
-          tmem_ld_wait32(sv);
-          tmem_ld_wait32(pv);
-          float ds[32];
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tb, sv);
+        tmem_ld32(tb + kHalf, pv);
+        tmem_ld_wait32(sv);
+        tmem_ld_wait32(pv);
+        float ds[32];
 #pragma unroll
-          for (int u = 0; u < 32; u += 2) {
-            float y0, y1;
-            fma2(y0, y1, __uint_as_float(sv[u]), __uint_as_float(sv[u + 1]), sl2, nlse2);
-            float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-            if (need_mask) {
-              const int key = k0 + kc + u;
-              if (!(key < N && (!CAUSAL || key <= qrow))) p0 = 0.f;
-              if (!(key + 1 < N && (!CAUSAL || key + 1 <= qrow))) p1 = 0.f;
-            }
-            float t0 = __uint_as_float(pv[u]), t1 = __uint_as_float(pv[u + 1]);
-            add2(t0, t1, ndelta, ndelta);
-            mul2v(ds[u], ds[u + 1], t0, t1, p0, p1);
+        for (int e = 0; e < 32; e += 2) {
+          float y0, y1;
+          fma2(y0, y1, __uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), sl2, nlse2);
+          float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          if (need_mask) {
+            const int key = k0 + e;
+            if (!(key < N && (!CAUSAL || key <= qrow))) p0 = 0.f;
+            if (!(key + 1 < N && (!CAUSAL || key + 1 <= qrow))) p1 = 0.f;
           }
-          uint32_t hi[16];
+          float t0 = __uint_as_float(pv[e]), t1 = __uint_as_float(pv[e + 1]);
+          add2(t0, t1, ndelta, ndelta);
+          mul2v(ds[e], ds[e + 1], t0, t1, p0, p1);
+        }
+        uint32_t hi[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) hi[u] = pack_bf16x2(ds[2 * u], ds[2 * u + 1]);
-          tmem_st16(tmem + L::kColS + lane_off + kc, hi);
-          if constexpr (SPLIT) {
-            uint32_t lo[16];
+        for (int e = 0; e < 16; ++e) hi[e] = pack_bf16x2(ds[2 * e], ds[2 * e + 1]);
+        tmem_st16(tb, hi);
+        if constexpr (SPLIT) {
+          uint32_t lo[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u)
-              lo[u] = pack_bf16x2(ds[2 * u] - bf16lo_to_f32(hi[u]), ds[2 * u + 1] - bf16hi_to_f32(hi[u]));
-            tmem_st16(tmem + L::kColS + lane_off + kc + 16, lo);
-          }
+          for (int e = 0; e < 16; ++e)
+            lo[e] = pack_bf16x2(ds[2 * e] - bf16lo_to_f32(hi[e]), ds[2 * e + 1] - bf16hi_to_f32(hi[e]));
+          tmem_st16(tb + 16, lo);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bDSReady));
+        if (lane == 0) mbar_arrive(bar(L::bDSReady + (u & 1)));
       }
       // ---------------- epilogue: dQ = alpha (sum of dS K) -> BF16 ----------------
       if (ok) ok = wait_warp(bar(L::bDQDone), 0, ctl);
       if (ok) {
         tc_fence_after();
-        constexpr int kCols = D / 2;   // this warp's dQ columns [kCols half, kCols half + kCols)
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.dq) + rowi * D + kCols * half;
+        constexpr int kCols = D / 2;   // this warp's dQ columns [kCols c, kCols c + kCols)
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.dq) + rowi * D + kCols * c;
 #pragma unroll 1
-        for (int c = 0; c < kCols; c += 32) {
+        for (int cc = 0; cc < kCols; cc += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + L::kColDQ + lane_off + kCols * half + c, v);
+          tmem_ld32(tmem + L::kColDQ + lane_off + kCols * c + cc, v);
           tmem_ld_wait32(v);
           if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            uint4* dst = reinterpret_cast<uint4*>(out + cc);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              auto f = [&](int e) { return sh.scale * __uint_as_float(v[8 * u + e]); };
-              dst[u] = make_uint4(pack_bf16x2(f(0), f(1)), pack_bf16x2(f(2), f(3)), pack_bf16x2(f(4), f(5)),
+            for (int q = 0; q < 4; ++q) {
+              auto f = [&](int e) { return sh.scale * __uint_as_float(v[8 * q + e]); };
+              dst[q] = make_uint4(pack_bf16x2(f(0), f(1)), pack_bf16x2(f(2), f(3)), pack_bf16x2(f(4), f(5)),
                                   pack_bf16x2(f(6), f(7)));
             }
           }
