@@ -497,6 +497,34 @@ def cpu_baseline(sample_heads=48, seed=0, min_seconds=0.0, max_reps=30):
             "seconds": dt}
 
 
+def cpu_workloads():
+    """The oracle (float64 numpy, as it stands) on one (batch, query head) slice of each
+    other configured workload -- forward in the workload's last mode, delta and backward --
+    and the time that scales linearly to the whole workload (every head costs the same)."""
+    import oracle
+    from precision_flash_attention_gb300 import inputs
+    out = {}
+    for name in ("tiny", "sink", "long", "gqa"):
+        wl = inputs.WORKLOADS[name]
+        t = inputs.make(name, seed=0)
+        g = wl.H_q // wl.H_kv
+        a = {n: x[:1, :1].to(torch.float64).numpy() for n, x in t.items() if n in ("q", "do")}
+        a.update({n: x[:1, :1].to(torch.float64).numpy() for n, x in t.items() if n in ("k", "v")})
+        t0 = time.perf_counter()
+        f = oracle.attn_fwd(a["q"], a["k"], a["v"], causal=wl.causal, scale=wl.alpha,
+                            fix_mode=wl.modes[-1], beta=wl.beta, eps=wl.eps)
+        dl = oracle.attn_delta(f["o"], a["do"])
+        oracle.attn_bwd(a["q"], a["k"], a["v"], a["do"], f["lse"], dl, causal=wl.causal,
+                        scale=wl.alpha)
+        dt = time.perf_counter() - t0
+        heads = wl.B * wl.H_q
+        fl = wl.flops() / heads
+        out[name] = {"slice": f"1 of {heads} (b, h) heads" + (f" (group of {g} shares K, V)" if g > 1 else ""),
+                     "slice_seconds": dt, "tflops": fl / dt / 1e12,
+                     "extrapolated_seconds_full_workload": dt * heads}
+    return out
+
+
 def _progress(args, msg):
     if args.progress:
         print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
@@ -681,6 +709,8 @@ def run_gpu_arm(args):
         return
     _progress(args, "e2e done; CPU baseline")
     cpu = cpu_baseline(sample_heads=48, min_seconds=10.0)
+    if args.sweep:
+        cpu["workloads"] = cpu_workloads()
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
