@@ -548,6 +548,9 @@ def run_gpu_arm(args):
     w = dict(WORKLOAD)
     if args.n:
         w["N"] = args.n
+    if args.d:
+        w["d"] = args.d
+        w["scale"] = 1.0 / math.sqrt(args.d)
     peaks = load_peaks()
     t = make_inputs(dev, w["B"], w["H"], w["N"], w["d"], seed=rank)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -780,6 +783,9 @@ def main():
     ap.add_argument("--mode", type=int, default=1, choices=[0, 1, 2])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--n", type=int, default=0, help="override the sequence length (profiling)")
+    ap.add_argument("--d", type=int, default=0, choices=[0, 64, 128],
+                    help="override the head dimension, scale 1/sqrt(d) (profiling; d = 128 runs the "
+                         "query-outer dQ pass)")
     ap.add_argument("--progress", action="store_true", help="log each stage to stderr")
     ap.add_argument("--kernels-only", action="store_true",
                     help="launch only the timed steps (for ncu captures); prints nothing")
