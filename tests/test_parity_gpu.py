@@ -460,6 +460,39 @@ def test_bwd_accumulate_entry_point(shape):
     assert st == -1 and "INVALID_ARG" in pfa.status_string(st)
 
 
+@pytest.mark.parametrize("d,B,H", [(64, 32, 512), (128, 16, 512)], ids=["d64", "d128"])
+def test_maximum_size(d, B, H):
+    # The largest problem the size checks accept: B * H * N * d just under 2^31 values per
+    # tensor, 4 GiB of BF16, so the byte offsets of the last heads need 33 bits. P distinct
+    # seeded heads are tiled over all B * H heads on the device; the first and last heads are
+    # checked against the oracle of their pattern, and equal patterns must give equal bits
+    # wherever the arithmetic does not depend on arrival order (O, lse, dK, dV).
+    N, P = 2047, 4
+    assert 2 ** 31 - 2 ** 21 < B * H * N * d < 2 ** 31
+    small = inputs.gaussian(1, P, P, N, d, std_qkv=0.5, std_do=1.0, seed=5)
+    full = {n: x.cuda().repeat(1, B * H // P, 1, 1).view(B, H, N, d) for n, x in small.items()}
+    scale = 1.0 / math.sqrt(d)
+    o, lse = pfa.forward(full["q"], full["k"], full["v"], causal=True, scale=scale, fix_mode=1)
+    dq, dk, dv, _ = pfa.backward(full["q"], full["k"], full["v"], o, lse, full["do"], causal=True,
+                                 scale=scale)
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    del full
+    ref = oracle_full(small, causal=True, scale=scale, fix_mode=1)
+    n_heads = B * H
+    for idx in (0, 1, 2, 3, n_heads // 2 + 1, n_heads - 4, n_heads - 3, n_heads - 2, n_heads - 1):
+        b, h = divmod(idx, H)
+        got = {n: f64(t[b, h]) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        want = {n: ref[n][0, idx % P] for n in ("o", "lse", "dq", "dk", "dv")}
+        assert_fwd_close(got, want, f"head {idx}")
+        assert_bwd_close(got, want, f"head {idx}")
+    last = divmod(n_heads - P, H)
+    for t in (o, lse, dk, dv):
+        assert torch.equal(t[0, 0], t[last[0], last[1]])
+    del o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+
+
 def test_cuda_graph_capture_matches_eager():
     # The calls allocate nothing and never synchronise, so a whole step (forward, delta,
     # backward with its zeroing and conversion, launched as programmatic dependents)
