@@ -179,6 +179,26 @@ def test_ragged_shapes(shape, mode):
     assert got["counters"]["nonfinite_rows"] == 0
 
 
+@pytest.mark.parametrize("N", [1, 2, 17])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_degenerate_lengths(N, d, causal):
+    # Sequences shorter than one 128-row tile, down to a single key: row 0 of a causal row
+    # sees only itself (one score, never repeated); everything past N is masked or zero-filled.
+    t = inputs.gaussian(2, 2, 1, N, d, std_qkv=0.8, std_do=1.0, seed=N + d)
+    scale = 1.0 / math.sqrt(d)
+    for mode in (0, 1, 2):
+        got = run_gpu(t, causal=causal, scale=scale, fix_mode=mode, beta=2.0)
+        ref = oracle_full(t, causal=causal, scale=scale, fix_mode=mode, beta=2.0)
+        assert_fwd_close(got, ref, f"N {N} d {d} mode {mode}")
+        assert_bwd_close(got, ref, f"N {N} d {d} mode {mode}")
+        # Float scores: a tie or a round-to-one decision may sit within FP32 rounding of its
+        # threshold, so the counts may differ by one; nothing is non-finite.
+        for n in ("repeated_rows", "ones"):
+            assert abs(got["counters"][n] - ref["counters"][n]) <= 1, (n, got["counters"], ref["counters"])
+        assert got["counters"]["nonfinite_rows"] == 0
+
+
 def test_delta_alt_equals_delta():
     # rowsum(dP o P) and rowsum(dO o O) agree (the identity of the paper's §3.2).
     t = inputs.gaussian(2, 4, 2, 333, 64, std_qkv=0.5, std_do=1.0, seed=3)
