@@ -1,7 +1,8 @@
 """Benchmark: stabilised BF16 attention forward + backward TFLOP/s on GB300.
 
-One step = forward (pfa_attn_fwd) + delta (pfa_attn_delta) + backward
-(pfa_attn_bwd, which also zeroes and converts its dQ workspace) over one batch
+One step = forward (pfa_attn_fwd) + delta (pfa_attn_delta_zero, which also zeroes
+the dQ workspace) + backward (pfa_attn_bwd_ex without its zeroing pass; it converts
+the dQ workspace to BF16) over one batch
 of the GPT-2-small attention layer (B=8, H=12, N=1024, d=64, causal), inputs
 resident in HBM, L2 flushed between steps. Algorithmic FLOPs per step:
 14 * B * H * N^2 * d / 2 (S, Pbar V forward; S, dP, dV, dK, dQ backward; causal).
@@ -31,9 +32,9 @@ WORKLOAD = dict(B=8, H=12, N=1024, d=64, causal=True, scale=0.125, beta=2.0, eps
 L2_FLUSH_BYTES = 256 << 20
 # The timed region spans at least this long, so the clock record holds several samples.
 TIMED_REGION_MIN_S = 0.06
-# Kernels of ours launched per step: attn_fwd, delta, the dQ workspace zeroing,
-# attn_bwd and the dQ conversion.
-LAUNCHES_PER_STEP = 5
+# Kernels of ours launched per step: attn_fwd, delta (which also zeroes the dQ
+# workspace), attn_bwd and the dQ conversion.
+LAUNCHES_PER_STEP = 4
 
 
 def flops(B, H, N, d, causal, which="fwd+bwd"):
@@ -258,6 +259,10 @@ class Step:
         self.dq, self.dk, self.dv = (torch.empty_like(t[n]) for n in ("q", "k", "v"))
         self.ws = torch.empty(pfa.bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
                               device=q.device)
+        # As pfa.backward does: at d = 64 with delta = rowsum(dO o O), the delta pass also
+        # zeroes the dQ workspace (pfa_attn_delta_zero) and the backward call skips its own
+        # zeroing pass.
+        self.fused_zero = delta_mode == 0 and d == 64
 
     def fwd(self):
         t = self.t
@@ -265,7 +270,10 @@ class Step:
 
     def delta_(self):
         if self.delta_mode == 0:
-            self.pfa.attn_delta(self.o, self.t["do"], self.delta)
+            if self.fused_zero:
+                self.pfa.attn_delta_zero(self.o, self.t["do"], self.delta, self.ws)
+            else:
+                self.pfa.attn_delta(self.o, self.t["do"], self.delta)
         else:
             self.delta_alt_(self.delta)
 
@@ -277,7 +285,7 @@ class Step:
     def bwd(self):
         t = self.t
         self.pfa.attn_bwd(t["q"], t["k"], t["v"], t["do"], self.lse, self.delta, self.dq, self.dk,
-                          self.dv, self.ws, **self.kw)
+                          self.dv, self.ws, workspace_zeroed=self.fused_zero, **self.kw)
 
     def bwd_ex(self, flags):
         """The backward call with pfa_attn_bwd_ex options (the query-outer dQ pass)."""
@@ -373,7 +381,8 @@ def measure_workload(name, device, steps, flush, peaks):
     modes = (0, 1, 2) if name == "gpt2" else wl.modes
     peak, hbm = peaks["bf16_tflops"], peaks["hbm_gbs"]
     f_fwd, f_bwd, f_tot, f_alt = (wl.flops(w) for w in ("fwd", "bwd", "fwd+bwd", "delta_alt"))
-    dl_bytes = B * Hq * N * (4 * d + 4)
+    # delta reads O and dO and writes delta; at d = 64 the same pass zeroes the dQ workspace.
+    dl_bytes = B * Hq * N * (4 * d + 4 + (4 * d if d == 64 else 0))
     out = {}
     for m in modes:
         st = Step(t, causal=wl.causal, scale=wl.alpha, fix_mode=m, beta=wl.beta, eps=wl.eps,
@@ -639,7 +648,8 @@ def run_gpu_arm(args):
     fwd_ms, dl_ms, bwd_ms, bk_ms = (mean(split[head][k])
                                     for k in ("fwd_ms", "delta_ms", "bwd_ms", "bwd_kernel_ms"))
     f_fwd, f_bwd = flops(B, H, N, d, True, "fwd"), flops(B, H, N, d, True, "bwd")
-    dl_bytes = B * H * N * (4 * d + 4)
+    # delta reads O and dO and writes delta; at d = 64 the same pass zeroes the dQ workspace.
+    dl_bytes = B * H * N * (4 * d + 4 + (4 * d if d == 64 else 0))
     kernels = {
         "attn_fwd": {"ms": fwd_ms, "TFLOP/s": f_fwd / fwd_ms / 1e9,
                      "frac_bf16_peak": f_fwd / fwd_ms / 1e9 / peak},
@@ -647,7 +657,8 @@ def run_gpu_arm(args):
                        "frac_hbm_peak": dl_bytes / dl_ms / 1e6 / peaks["hbm_gbs"]},
         "attn_bwd": {"ms": bwd_ms, "TFLOP/s": f_bwd / bwd_ms / 1e9,
                      "frac_bf16_peak": f_bwd / bwd_ms / 1e9 / peak,
-                     "note": "the pfa_attn_bwd call: workspace zeroing, kernel, dQ conversion"},
+                     "note": "the backward call: kernel and dQ conversion (the delta pass zeroed the "
+                             "workspace)"},
         "attn_bwd_kernel": {"ms": bk_ms, "TFLOP/s": f_bwd / bk_ms / 1e9,
                             "frac_bf16_peak": f_bwd / bk_ms / 1e9 / peak},
     }

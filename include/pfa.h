@@ -163,6 +163,17 @@ int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa
 int pfa_attn_delta(const pfa_bf16* o, const pfa_bf16* dO, float* delta, int B, int H_q, int N,
                    int d, pfa_stream_t stream);
 
+/* pfa_attn_delta, and in the same pass the dQ workspace of pfa_attn_bwd zeroed (no
+ * counterpart in the paper): the workspace's row (b, h, i) of d FP32 values is
+ * cleared by the threads that read row i of O and dO, so the backward call can skip
+ * its own zeroing pass (pfa_attn_bwd_ex with PFA_BWD_WORKSPACE_ZEROED), one pass over
+ * memory fewer per step. Useful at d = 64, where pfa_attn_bwd uses the workspace.
+ *   o, dO [B,H_q,N,d] (in); delta [B,H_q,N] (out);
+ *   dq_accum: the workspace, at least B*H_q*N*d FP32 values, 16-byte aligned (out: zero).
+ * Same checks and errors as pfa_attn_delta; dq_accum NULL is PFA_ERR_INVALID_ARG. */
+int pfa_attn_delta_zero(const pfa_bf16* o, const pfa_bf16* dO, float* delta, float* dq_accum, int B,
+                        int H_q, int N, int d, pfa_stream_t stream);
+
 /* delta = rowsum(dP o P) with P = exp(alpha Q K^T - lse) and dP = dO V^T
  * recomputed: the mathematically equal alternative of [PK] method, paper §3.2.
  *   q, dO [B,H_q,N,d], k, v [B,H_kv,N,d], lse [B,H_q,N] (in); delta (out). */
@@ -210,9 +221,14 @@ int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
                                        keys that share a large feature get nearly cancelling dS
                                        (a sink key copied into other positions), where the single
                                        BF16 cast of dS dominates the error of dQ. */
+#define PFA_BWD_WORKSPACE_ZEROED 4u /* (the reduce-add dQ of pfa_attn_bwd) the caller vouches that
+                                       dq_accum holds zeros, as pfa_attn_delta_zero on the same
+                                       stream leaves it; the zeroing pass is skipped. Ignored
+                                       by the query-outer pass, which uses no workspace. */
 
 /* The backward pass of pfa_attn_bwd with options (no counterpart in the paper).
- * flags == 0 is pfa_attn_bwd exactly. With PFA_BWD_DQ_DETERMINISTIC or
+ * flags == 0 is pfa_attn_bwd exactly; PFA_BWD_WORKSPACE_ZEROED alone is pfa_attn_bwd
+ * without its zeroing pass. With PFA_BWD_DQ_DETERMINISTIC or
  * PFA_BWD_DQ_SPLIT the key-outer kernel computes dK and dV only, and a
  * query-outer pass recomputes S, P, dP and dS per query tile to form
  * dQ = alpha dS K (the equation of pfa_attn_bwd, [PK] equations): it costs two

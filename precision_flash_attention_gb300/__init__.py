@@ -15,16 +15,16 @@ import math
 
 import torch
 
-from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, EXPORTS, FWD_PBAR_E4M3, FWD_PBAR_MXFP4,
+from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, BWD_WORKSPACE_ZEROED, EXPORTS, FWD_PBAR_E4M3, FWD_PBAR_MXFP4,
                    FWD_UNFUSED_BF16_PV, MONITOR_WORDS,
                    TIE_BINS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_ex, attn_bwd_noalloc,
-                   attn_delta, attn_delta_alt, attn_fwd, attn_fwd_ex, bwd_workspace_bytes,
+                   attn_delta, attn_delta_alt, attn_delta_zero, attn_fwd, attn_fwd_ex, bwd_workspace_bytes,
                    device_error, device_error_site, load, status_string, wait_probe)
 
 __all__ = [
-    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "EXPORTS", "FWD_PBAR_E4M3", "FWD_PBAR_MXFP4",
+    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "BWD_WORKSPACE_ZEROED", "EXPORTS", "FWD_PBAR_E4M3", "FWD_PBAR_MXFP4",
     "FWD_UNFUSED_BF16_PV", "MONITOR_WORDS",
-    "TIE_BINS", "PfaError", "attn_fwd", "attn_fwd_ex", "attn_delta",
+    "TIE_BINS", "PfaError", "attn_fwd", "attn_fwd_ex", "attn_delta", "attn_delta_zero",
     "attn_delta_alt", "attn_bwd", "attn_bwd_accum", "attn_bwd_ex", "attn_bwd_noalloc",
     "bwd_workspace_bytes", "device_error", "device_error_site", "load", "status_string", "wait_probe",
     "forward", "backward",
@@ -74,25 +74,31 @@ def backward(q, k, v, o, lse, do, *, causal=False, scale=None, delta_mode=0, dq_
 
     ``dq_mode``: "atomic" (pfa_attn_bwd: per-key-tile dQ sums reduce-added into an FP32
     workspace), "deterministic" (the query-outer dQ pass) or "split" (the query-outer pass
-    with dS as a BF16 hi + lo pair). Returns (dq, dk, dv, delta)."""
+    with dS as a BF16 hi + lo pair). With "atomic" at d = 64 and delta = rowsum(dO o O), the
+    delta pass also zeroes the workspace (pfa_attn_delta_zero) and the backward call skips
+    its own zeroing pass. Returns (dq, dk, dv, delta)."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
     flags = DQ_MODES[dq_mode]
+    B, H, N, d = q.shape
     delta = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fused_zero = flags == 0 and delta_mode == 0 and d == 64
+    if flags == 0 and workspace is None:
+        workspace = torch.empty(bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
+                                device=q.device)
     if delta_mode == 0:
-        attn_delta(o, do, delta, stream=stream)
+        if fused_zero:
+            attn_delta_zero(o, do, delta, workspace, stream=stream)
+        else:
+            attn_delta(o, do, delta, stream=stream)
     else:
         attn_delta_alt(q, k, v, do, lse, delta, causal=causal, scale=scale, stream=stream)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    B, H, N, d = q.shape
     if flags:
         attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, None, causal=causal, scale=scale,
                     flags=flags, stream=stream)
         return dq, dk, dv, delta
-    if workspace is None:
-        workspace = torch.empty(bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32,
-                                device=q.device)
     attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, workspace, causal=causal, scale=scale,
-             stream=stream)
+             stream=stream, workspace_zeroed=fused_zero)
     return dq, dk, dv, delta
 
 

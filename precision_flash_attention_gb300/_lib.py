@@ -26,12 +26,13 @@ MONITOR_WORDS = 1 + TIE_BINS
 # pfa_attn_bwd_ex flags (include/pfa.h)
 BWD_DQ_DETERMINISTIC = 1
 BWD_DQ_SPLIT = 2
+BWD_WORKSPACE_ZEROED = 4
 STATUS_NAMES = {0: "PFA_OK", -1: "PFA_ERR_INVALID_ARG", -2: "PFA_ERR_MISALIGNED",
                 -3: "PFA_ERR_UNSUPPORTED", -4: "PFA_ERR_LAUNCH", -5: "PFA_ERR_DEVICE",
                 -6: "PFA_ERR_TOO_LARGE"}
 
 # Every entry point declared in include/pfa.h.
-EXPORTS = ("pfa_attn_fwd", "pfa_attn_fwd_ex", "pfa_attn_delta", "pfa_attn_delta_alt", "pfa_attn_bwd",
+EXPORTS = ("pfa_attn_fwd", "pfa_attn_fwd_ex", "pfa_attn_delta", "pfa_attn_delta_zero", "pfa_attn_delta_alt", "pfa_attn_bwd",
            "pfa_attn_bwd_accum", "pfa_attn_bwd_ex", "pfa_attn_bwd_noalloc", "pfa_bwd_workspace_bytes", "pfa_status_string",
            "pfa_last_error", "pfa_device_error", "pfa_device_error_site", "pfa_wait_probe")
 
@@ -66,6 +67,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pfa_attn_fwd_ex.restype = i
     lib.pfa_attn_delta.argtypes = [vp, vp, vp, i, i, i, i, vp]
     lib.pfa_attn_delta.restype = i
+    lib.pfa_attn_delta_zero.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+    lib.pfa_attn_delta_zero.restype = i
     lib.pfa_attn_delta_alt.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
     lib.pfa_attn_delta_alt.restype = i
     lib.pfa_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
@@ -221,6 +224,27 @@ def attn_delta(o, do, delta, *, stream=None) -> None:
     _check(st, "pfa_attn_delta")
 
 
+def attn_delta_zero(o, do, delta, dq_accum, *, stream=None) -> None:
+    """pfa_attn_delta_zero: delta = rowsum(dO o O), and the first B*H_q*N*d values of the
+    FP32 dQ workspace ``dq_accum`` zeroed in the same pass (then attn_bwd may skip its
+    zeroing pass: ``workspace_zeroed=True``)."""
+    _layout(o, "o")
+    _layout(do, "do")
+    _layout(delta, "delta", torch.float32, 3)
+    B, Hq, N, d = o.shape
+    _expect(do, "do", o.shape)
+    _expect(delta, "delta", (B, Hq, N))
+    if (not isinstance(dq_accum, torch.Tensor) or dq_accum.dtype != torch.float32
+            or not dq_accum.is_contiguous()):
+        raise ValueError("dq_accum must be a contiguous float32 tensor")
+    if dq_accum.numel() < o.numel():
+        raise ValueError("dq_accum is smaller than B*H_q*N*d values")
+    _on_device((o, "o"), (do, "do"), (delta, "delta"), (dq_accum, "dq_accum"))
+    st = load().pfa_attn_delta_zero(_ptr(o), _ptr(do), _ptr(delta), _ptr(dq_accum), B, Hq, N, d,
+                                    _stream(stream))
+    _check(st, "pfa_attn_delta_zero")
+
+
 def attn_delta_alt(q, k, v, do, lse, delta, *, causal: bool, scale: float, stream=None) -> None:
     """pfa_attn_delta_alt: delta = rowsum(dP o P) with P, dP recomputed."""
     B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do")],
@@ -236,8 +260,11 @@ def bwd_workspace_bytes(B: int, H_q: int, N: int, d: int) -> int:
 
 
 def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, scale: float,
-             stream=None) -> None:
-    """pfa_attn_bwd: dQ, dK, dV from lse and delta (dq_accum is the FP32 workspace)."""
+             stream=None, workspace_zeroed: bool = False) -> None:
+    """pfa_attn_bwd: dQ, dK, dV from lse and delta (dq_accum is the FP32 workspace).
+    ``workspace_zeroed`` (pfa_attn_bwd_ex with BWD_WORKSPACE_ZEROED): the caller vouches that
+    the workspace holds zeros (attn_delta_zero on the same stream), and the zeroing pass is
+    skipped."""
     if (not isinstance(dq_accum, torch.Tensor) or dq_accum.dtype != torch.float32
             or not dq_accum.is_contiguous()):
         raise ValueError("dq_accum must be a contiguous float32 tensor")
@@ -246,6 +273,13 @@ def attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, sca
     B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do"), (dq, "dq")],
                                   extra_k=[(dk, "dk"), (dv, "dv")],
                                   rows=[(lse, "lse"), (delta, "delta")], also=[(dq_accum, "dq_accum")])
+    if workspace_zeroed:
+        st = load().pfa_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, Hkv, N, d,
+                                    int(bool(causal)), float(scale), BWD_WORKSPACE_ZEROED,
+                                    _stream(stream))
+        _check(st, "pfa_attn_bwd_ex")
+        return
     st = load().pfa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse), _ptr(delta), _ptr(dq),
                              _ptr(dk), _ptr(dv), _ptr(dq_accum), B, Hq, Hkv, N, d,
                              int(bool(causal)), float(scale), _stream(stream))
@@ -257,10 +291,12 @@ def attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, *, causal: bool, 
     """pfa_attn_bwd_ex: pfa_attn_bwd with options. ``flags`` 0 is attn_bwd (dq_accum the FP32
     workspace); BWD_DQ_DETERMINISTIC and/or BWD_DQ_SPLIT compute dQ by the query-outer pass
     (dq_accum unused, may be None)."""
-    if flags == 0:
+    known = BWD_DQ_DETERMINISTIC | BWD_DQ_SPLIT | BWD_WORKSPACE_ZEROED
+    if (flags & ~known) == 0 and (flags & (BWD_DQ_DETERMINISTIC | BWD_DQ_SPLIT)) == 0:
         attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, dq_accum, causal=causal, scale=scale,
-                 stream=stream)
+                 stream=stream, workspace_zeroed=bool(flags & BWD_WORKSPACE_ZEROED))
         return
+    # The query-outer pass needs no workspace (unknown flag bits are the library's to refuse).
     B, Hq, Hkv, N, d = _check_qkv(q, k, v, extra_q=[(do, "do"), (dq, "dq")],
                                   extra_k=[(dk, "dk"), (dv, "dv")],
                                   rows=[(lse, "lse"), (delta, "delta")])

@@ -275,6 +275,19 @@ int pfa_attn_delta(const pfa_bf16* o, const pfa_bf16* dO, float* delta, int B, i
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int pfa_attn_delta_zero(const pfa_bf16* o, const pfa_bf16* dO, float* delta, float* dq_accum, int B,
+                        int H_q, int N, int d, pfa_stream_t stream) {
+  if (!o || !dO || !delta || !dq_accum) return PFA_ERR_INVALID_ARG;
+  int rc = check_sizes(B, H_q, H_q, N, d);
+  if (rc != PFA_OK) return rc;
+  if (!aligned16(o) || !aligned16(dO) || !aligned16(delta) || !aligned16(dq_accum))
+    return PFA_ERR_MISALIGNED;
+  DeviceState* dev = nullptr;
+  if ((rc = current_device(&dev)) != PFA_OK) return rc;
+  return launched(pfa::launch_delta(o, dO, delta, static_cast<long long>(B) * H_q * N, d,
+                                    reinterpret_cast<cudaStream_t>(stream), dq_accum));
+}
+
 int pfa_attn_delta_alt(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
                        const float* lse, float* delta, int B, int H_q, int H_kv, int N, int d,
                        int causal, float scale, pfa_stream_t stream) {
@@ -393,10 +406,16 @@ int bwd_query_outer(const BwdLaunch& L, pfa_bf16* dq, const float* lse, const fl
 
 extern "C" {
 
-int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
-                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
-                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
-                 pfa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// pfa_attn_bwd; zeroed: the caller vouches that the workspace holds zeros (as
+// pfa_attn_delta_zero leaves it), and the zeroing pass is skipped.
+int bwd_key_outer(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                  const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                  float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                  bool zeroed, pfa_stream_t stream) {
   if (!dq) return PFA_ERR_INVALID_ARG;
   int rc = bwd_check(q, k, v, dO, lse, delta, dq_accum, dk, dv, B, H_q, H_kv, N, d, scale);
   if (rc != PFA_OK) return rc;
@@ -411,10 +430,23 @@ int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const 
   // (and deterministic), so it computes dQ and the workspace is not used.
   if (d == 128) return bwd_query_outer(L, dq, lse, delta, /*split=*/false, st);
   const size_t ws = pfa_bwd_workspace_bytes(B, H_q, N, d);
-  if ((rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
+  if (!zeroed &&
+      (rc = launched(pfa::launch_zero_workspace(dq_accum, static_cast<long long>(ws / 16), st))) != PFA_OK)
     return rc;
   if ((rc = bwd_launch(L, st)) != PFA_OK) return rc;
   return launched(pfa::launch_convert_dq(dq_accum, dq, static_cast<long long>(ws / sizeof(float)), st));
+}
+
+}  // namespace
+
+extern "C" {
+
+int pfa_attn_bwd(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
+                 const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
+                 float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
+                 pfa_stream_t stream) {
+  return bwd_key_outer(q, k, v, dO, lse, delta, dq, dk, dv, dq_accum, B, H_q, H_kv, N, d, causal,
+                       scale, false, stream);
 }
 
 int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
@@ -433,11 +465,11 @@ int pfa_attn_bwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, con
                     const float* lse, const float* delta, pfa_bf16* dq, pfa_bf16* dk, pfa_bf16* dv,
                     float* dq_accum, int B, int H_q, int H_kv, int N, int d, int causal, float scale,
                     unsigned flags, pfa_stream_t stream) {
-  if (flags & ~static_cast<unsigned>(PFA_BWD_DQ_DETERMINISTIC | PFA_BWD_DQ_SPLIT))
+  if (flags & ~static_cast<unsigned>(PFA_BWD_DQ_DETERMINISTIC | PFA_BWD_DQ_SPLIT | PFA_BWD_WORKSPACE_ZEROED))
     return PFA_ERR_INVALID_ARG;
-  if (flags == 0)
-    return pfa_attn_bwd(q, k, v, dO, lse, delta, dq, dk, dv, dq_accum, B, H_q, H_kv, N, d, causal,
-                        scale, stream);
+  if ((flags & (PFA_BWD_DQ_DETERMINISTIC | PFA_BWD_DQ_SPLIT)) == 0)
+    return bwd_key_outer(q, k, v, dO, lse, delta, dq, dk, dv, dq_accum, B, H_q, H_kv, N, d, causal,
+                         scale, (flags & PFA_BWD_WORKSPACE_ZEROED) != 0, stream);
   // The query-outer pass computes dQ; the key-outer kernel only dK and dV.
   if (!dq) return PFA_ERR_INVALID_ARG;
   int rc = bwd_check(q, k, v, dO, lse, delta, nullptr, dk, dv, B, H_q, H_kv, N, d, scale, false);

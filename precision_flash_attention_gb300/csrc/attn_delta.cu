@@ -14,10 +14,14 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TPR threads per row, each loading 8 BF16 values (16 bytes) of O and of dO.
+// zero_ws non-null: the row's d FP32 values of the dQ workspace are zeroed in the
+// same pass (each thread writes the 32 bytes that match its 16 of O and dO), so
+// that the backward call can skip its own zeroing pass.
 template <int TPR>
 __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
                                                     const uint4* __restrict__ dO,
-                                                    float* __restrict__ delta, long long rows) {
+                                                    float* __restrict__ delta, long long rows,
+                                                    float4* __restrict__ zero_ws) {
   constexpr int kRowsPerBlock = 256 / TPR;
   const int sub = threadIdx.x % TPR;
   grid_launch_dependents();
@@ -37,6 +41,11 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
       for (int u = 0; u < 4; ++u) {
         acc = fmaf(bf16lo_to_f32(av[u]), bf16lo_to_f32(gv[u]), acc);
         acc = fmaf(bf16hi_to_f32(av[u]), bf16hi_to_f32(gv[u]), acc);
+      }
+      if (zero_ws != nullptr) {
+        float4* w = zero_ws + row * (2 * TPR) + 2 * sub;
+        w[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        w[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
@@ -242,7 +251,7 @@ cudaError_t launch_alt_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long rows, int d,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, float* zero_ws) {
   const int threads = 256;
   const int tpr = d / 8;
   const long long rows_per_block = threads / tpr;
@@ -252,9 +261,9 @@ cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long 
   const dim3 grid(static_cast<unsigned>(blocks));
   if (d == 64)
     return launch_pdl(delta_kernel<8>, grid, dim3(threads), 0, stream, static_cast<const uint4*>(o),
-                      static_cast<const uint4*>(dO), delta, rows);
+                      static_cast<const uint4*>(dO), delta, rows, reinterpret_cast<float4*>(zero_ws));
   return launch_pdl(delta_kernel<16>, grid, dim3(threads), 0, stream, static_cast<const uint4*>(o),
-                    static_cast<const uint4*>(dO), delta, rows);
+                    static_cast<const uint4*>(dO), delta, rows, reinterpret_cast<float4*>(zero_ws));
 }
 
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -103,8 +103,10 @@ cudaError_t launch_fwd_study(const CUtensorMap& tq, const CUtensorMap& tk, const
 // The narrow Pbar formats (a.pbar 1 or 2; d = 64, monitor counted, profile or fused).
 cudaError_t launch_fwd_lowp(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& a, cudaStream_t stream);
+// delta = rowsum(dO o O) over `rows` rows of d values; zero_ws non-null: the matching
+// rows x d FP32 values of the dQ workspace are zeroed in the same pass.
 cudaError_t launch_delta(const void* o, const void* dO, float* delta, long long rows, int d,
-                         cudaStream_t stream);
+                         cudaStream_t stream, float* zero_ws = nullptr);
 cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const CUtensorMap& tdo, const DeltaAltArgs& a, cudaStream_t stream);
 // tdq: FP32 [B*Hq, N, d] map of the dQ workspace with 32-column x 32-row boxes and

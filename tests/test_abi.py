@@ -151,7 +151,10 @@ def test_bwd_ex_validates(lib):
     inv, mis = -1, -2
     args = [A] * 10 + [1, 2, 1, 64, 64, 1, 0.125, 0, None]
     bad = list(args)
-    bad[17] = 4                          # an unknown flag bit
+    bad[17] = 8                          # an unknown flag bit
+    assert lib.pfa_attn_bwd_ex(*bad) == inv
+    bad = list(args)
+    bad[17], bad[9] = 4, None            # a zeroed workspace is still a workspace
     assert lib.pfa_attn_bwd_ex(*bad) == inv
     bad = list(args)
     bad[17], bad[6] = 1, None            # the query-outer pass needs dq
@@ -187,3 +190,11 @@ def test_fwd_ex_validates(lib):
         for fl in (1, 2, 4, 1 | 2):
             assert call(flags=fl, d=128) == -3        # the study variants are d = 64 only
             assert call(flags=fl) not in (inv, mis)
+
+
+def test_delta_zero_validates(lib):
+    inv, mis = -1, -2
+    args = [A, A, A, A, 1, 2, 64, 64, None]
+    assert lib.pfa_attn_delta_zero(*args[:3], None, *args[4:]) == inv   # the workspace is required
+    assert lib.pfa_attn_delta_zero(*args[:3], A + 4, *args[4:]) == mis  # misaligned workspace
+    assert lib.pfa_attn_delta_zero(*args[:4], 1, 2, 64, 96, None) == inv  # d not 64 or 128

@@ -199,6 +199,23 @@ def test_degenerate_lengths(N, d, causal):
         assert got["counters"]["nonfinite_rows"] == 0
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_delta_zero_pass(d):
+    # pfa_attn_delta_zero gives pfa_attn_delta's delta bit for bit and leaves the first
+    # B*H*N*d values of the workspace zero (whatever they held), the rest untouched.
+    t = to_dev(inputs.gaussian(2, 3, 3, 200, d, std_qkv=0.5, std_do=1.0, seed=d))
+    o, lse = pfa.forward(t["q"], t["k"], t["v"], causal=True, scale=0.125)
+    d1, d2 = torch.empty_like(lse), torch.empty_like(lse)
+    ws = torch.full((t["q"].numel() + 64,), 7.0, dtype=torch.float32, device="cuda")
+    pfa.attn_delta(o, t["do"], d1)
+    pfa.attn_delta_zero(o, t["do"], d2, ws)
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    assert torch.equal(d1, d2)
+    assert int(torch.count_nonzero(ws[: t["q"].numel()])) == 0
+    assert bool((ws[t["q"].numel():] == 7.0).all())
+
+
 def test_delta_alt_equals_delta():
     # rowsum(dP o P) and rowsum(dO o O) agree (the identity of the paper's §3.2).
     t = inputs.gaussian(2, 4, 2, 333, 64, std_qkv=0.5, std_do=1.0, seed=3)
@@ -385,9 +402,12 @@ def test_bwd_ex_argument_errors():
     delta = torch.empty_like(lse)
     pfa.attn_delta(o, t["do"], delta)
     dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
-    with pytest.raises(pfa.PfaError, match="INVALID_ARG"):
+    with pytest.raises(pfa.PfaError, match="INVALID_ARG"):   # an unknown flag bit
         pfa.attn_bwd_ex(t["q"], t["k"], t["v"], t["do"], lse, delta, dq, dk, dv, None, causal=False,
-                        scale=0.125, flags=4)
+                        scale=0.125, flags=8)
+    with pytest.raises(ValueError, match="dq_accum"):         # a zeroed workspace is still required
+        pfa.attn_bwd_ex(t["q"], t["k"], t["v"], t["do"], lse, delta, dq, dk, dv, None, causal=False,
+                        scale=0.125, flags=pfa.BWD_WORKSPACE_ZEROED)
     assert pfa.device_error() == 0
 
 
