@@ -31,7 +31,7 @@ METRIC = "attention fwd+bwd TFLOP/s and % of GB300 BF16 peak (GPT-2 shape, N=1kâ
 WORKLOAD = dict(B=8, H=12, N=1024, d=64, causal=True, scale=0.125, beta=2.0, eps=1e-3)
 L2_FLUSH_BYTES = 256 << 20
 # The timed region spans at least this long, so the clock record holds several samples.
-TIMED_REGION_MIN_S = 0.06
+TIMED_REGION_MIN_S = 0.2
 # Kernels of ours launched per step: attn_fwd, delta (which also zeroes the dQ
 # workspace), attn_bwd and the dQ conversion.
 LAUNCHES_PER_STEP = 4
@@ -358,6 +358,33 @@ def time_step(step, steps, warmup, flush, split=False):
     return out
 
 
+def time_interleaved(steps_by_mode, k, flush):
+    """Whole steps of each mode in turn, k rounds, L2 flushed before each step and CUDA
+    events at each step's ends. Everything is enqueued before one synchronisation, so the
+    host runs ahead of the GPU and its own launch work never shows in the device times.
+    Returns the step times per mode (ms)."""
+    rec = {m: [] for m in steps_by_mode}
+    for _ in range(k):
+        for m, st in steps_by_mode.items():
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            st.run()
+            e1.record()
+            rec[m].append((e0, e1))
+    torch.cuda.synchronize()
+    return {m: [a.elapsed_time(b) for a, b in v] for m, v in rec.items()}
+
+
+def interleaved_step_ms(steps_by_mode, k, flush):
+    """Median whole-step time per mode, the modes interleaved step by step (one step of each
+    in turn, L2 flushed before each), so that they are compared under the same conditions."""
+    for st in steps_by_mode.values():
+        time_step(st, 1, 2, flush)
+    times = time_interleaved(steps_by_mode, k, flush)
+    return {m: statistics.median(v) for m, v in times.items()}
+
+
 # The other configured workloads, each timed in every mode it lists (tests check them against
 # the oracle; here they are measured). Mode 2 is added for the GPT-2 layer.
 OTHER_WORKLOADS = [
@@ -384,13 +411,14 @@ def measure_workload(name, device, steps, flush, peaks):
     # delta reads O and dO and writes delta; at d = 64 the same pass zeroes the dQ workspace.
     dl_bytes = B * Hq * N * (4 * d + 4 + (4 * d if d == 64 else 0))
     out = {}
+    sts = {m: Step(t, causal=wl.causal, scale=wl.alpha, fix_mode=m, beta=wl.beta, eps=wl.eps,
+                   delta_mode=1 if name == "sink" else 0) for m in modes}
+    splits = {m: time_step(sts[m], steps, 2, flush, split=True) for m in modes}
+    step_ms_all = interleaved_step_ms(sts, steps, flush)
     for m in modes:
-        st = Step(t, causal=wl.causal, scale=wl.alpha, fix_mode=m, beta=wl.beta, eps=wl.eps,
-                  delta_mode=1 if name == "sink" else 0)
-        r = time_step(st, steps, 2, flush, split=True)
-        tot = time_step(st, steps, 0, flush)["step_ms"]
+        r = splits[m]
         med = {k: statistics.median(v) for k, v in r.items()}
-        step_ms = statistics.median(tot)
+        step_ms = step_ms_all[m]
         e = {"fwd_ms": med["fwd_ms"], "bwd_call_ms": med["bwd_ms"], "bwd_kernel_ms": med["bwd_kernel_ms"],
              "step_ms": step_ms,
              "fwd_tflops": f_fwd / med["fwd_ms"] / 1e9,
@@ -413,8 +441,7 @@ def measure_workload(name, device, steps, flush, peaks):
         else:
             e["step_note"] = "step = fwd + delta_alt + bwd; total_tflops counts fwd+bwd FLOPs only"
         out[f"mode {m}"] = e
-        del st
-    del t
+    del sts, t
     torch.cuda.empty_cache()
     return {"shape": dict(B=B, H_q=Hq, H_kv=wl.H_kv, N=N, d=d, causal=wl.causal, alpha=wl.alpha,
                           beta=wl.beta, eps=wl.eps),
@@ -585,16 +612,19 @@ def run_gpu_arm(args):
         # several clock-sampling periods (a pass of the bench workload takes a few ms, less
         # than one period); the line reports K and the number of passes.
         def one_pass(res, log):
-            for it in range(args.steps):
-                for m in steps:
-                    r = time_step(steps[m], 1, 0, flush)
-                    for k2 in r:
-                        res[m][k2] += r[k2]
-                    if log and args.progress:
+            if log and args.progress:
+                # Diagnostic run: one step at a time, each checked for a device error.
+                for it in range(args.steps):
+                    for m in steps:
+                        r = time_step(steps[m], 1, 0, flush)
+                        res[m]["step_ms"] += r["step_ms"]
                         err = pfa.device_error()
                         _progress(args, f"step {it} mode {m}: {r['step_ms'][0]:.3f} ms, error word {err}"
                                         + (f", first timeout at {pfa.device_error_site()}" if err else ""))
-            torch.cuda.synchronize()
+                return
+            r = time_interleaved(steps, args.steps, flush)
+            for m in r:
+                res[m]["step_ms"] += r[m]
 
         passes = 1
         if not args.kernels_only:
@@ -681,14 +711,18 @@ def run_gpu_arm(args):
     if args.sweep and rank == 0:
         for n_s in (2048, 4096, 8192):
             ts = make_inputs(dev, B, H, n_s, d, seed=1)
-            tot_ms = {}
-            for m in (0, 1, 2):
+            k_s = max(3, args.steps // 2)
+            sts = {m: Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
+                   for m in (0, 1, 2)}
+            split_s = {}
+            for m in sts:
                 _progress(args, f"sweep N={n_s} mode {m}")
-                st = Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
-                r = time_step(st, max(3, args.steps // 2), 2, flush, split=True)
+                split_s[m] = time_step(sts[m], k_s, 2, flush, split=True)
+            tot_ms = interleaved_step_ms(sts, k_s, flush)
+            for m in (0, 1, 2):
+                r = split_s[m]
                 fm, bm, km = (statistics.median(r[k]) for k in ("fwd_ms", "bwd_ms", "bwd_kernel_ms"))
-                sm = statistics.median(time_step(st, max(3, args.steps // 2), 0, flush)["step_ms"])
-                tot_ms[m] = sm
+                sm = tot_ms[m]
                 tot = flops(B, H, n_s, d, True) / sm / 1e9
                 sweep[f"N={n_s},mode={m}"] = {
                     "fwd_tflops": flops(B, H, n_s, d, True, "fwd") / fm / 1e9,
@@ -697,8 +731,7 @@ def run_gpu_arm(args):
                     "total_tflops": tot, "total_frac_bf16_peak": tot / peak}
                 if m > 0:
                     sweep[f"N={n_s},mode={m}"]["overhead_vs_mode0_pct"] = 100.0 * (sm / tot_ms[0] - 1.0)
-                del st
-            del ts
+            del sts, ts
     workloads = {}
     if args.sweep and rank == 0:
         for name, label in OTHER_WORKLOADS:
