@@ -385,6 +385,48 @@ def interleaved_step_ms(steps_by_mode, k, flush):
     return {m: statistics.median(v) for m, v in times.items()}
 
 
+def measure_study(t, w, flush, k, peak):
+    """Forward time of the study variants of pfa_attn_fwd_ex on the bench workload (mode 1):
+    the fused kernel with its counters, the training-time monitor, the unfused BF16 Pbar V
+    profile and the FP8 E4M3 / MXFP4 Pbar formats. The variants are interleaved one call at
+    a time, L2 flushed before each, all enqueued before one synchronisation."""
+    import precision_flash_attention_gb300 as pfa
+    q = t["q"]
+    B, H, N, d = q.shape
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    cnt, mon = pfa.new_counters(q.device), pfa.new_monitor(q.device)
+    kw = dict(causal=True, scale=w["scale"], fix_mode=1, beta=w["beta"], eps=w["eps"])
+    variants = {
+        "fused": lambda: pfa.attn_fwd(q, t["k"], t["v"], o, lse, **kw),
+        "fused + counters": lambda: pfa.attn_fwd(q, t["k"], t["v"], o, lse, counters=cnt, **kw),
+        "monitor": lambda: pfa.attn_fwd_ex(q, t["k"], t["v"], o, lse, counters=cnt, monitor=mon, **kw),
+        "unfused BF16 Pbar V profile": lambda: pfa.attn_fwd_ex(
+            q, t["k"], t["v"], o, lse, monitor=mon, flags=pfa.FWD_UNFUSED_BF16_PV, **kw),
+        "Pbar FP8 E4M3": lambda: pfa.attn_fwd_ex(q, t["k"], t["v"], o, lse, monitor=mon,
+                                                 flags=pfa.FWD_PBAR_E4M3, **kw),
+        "Pbar MXFP4": lambda: pfa.attn_fwd_ex(q, t["k"], t["v"], o, lse, monitor=mon,
+                                              flags=pfa.FWD_PBAR_MXFP4, **kw),
+    }
+    for fn in variants.values():
+        for _ in range(2):
+            flush.fill_(1.0)
+            fn()
+    rec = {n: [] for n in variants}
+    for _ in range(k):
+        for n, fn in variants.items():
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            rec[n].append((e0, e1))
+    torch.cuda.synchronize()
+    f_fwd = flops(B, H, N, d, True, "fwd")
+    med = {n: statistics.median(a.elapsed_time(b) for a, b in v) for n, v in rec.items()}
+    return {n: {"fwd_ms": m, "fwd_tflops": f_fwd / m / 1e9, "fwd_frac_bf16_peak": f_fwd / m / 1e9 / peak,
+                "vs_fused_pct": 100.0 * (m / med["fused"] - 1.0)} for n, m in med.items()}
+
+
 # The other configured workloads, each timed in every mode it lists (tests check them against
 # the oracle; here they are measured). Mode 2 is added for the GPT-2 layer.
 OTHER_WORKLOADS = [
@@ -732,6 +774,10 @@ def run_gpu_arm(args):
                 if m > 0:
                     sweep[f"N={n_s},mode={m}"]["overhead_vs_mode0_pct"] = 100.0 * (sm / tot_ms[0] - 1.0)
             del sts, ts
+    study = None
+    if args.sweep and rank == 0 and w["d"] == 64:
+        _progress(args, "study variants")
+        study = measure_study(t, w, flush, max(5, args.steps // 2), peak)
     workloads = {}
     if args.sweep and rank == 0:
         for name, label in OTHER_WORKLOADS:
@@ -769,6 +815,7 @@ def run_gpu_arm(args):
         "timed_passes": passes, "clocks": clk.summary(), "wall_s_timed_region": wall,
         "kernels": kernels, "mode_tflops": mode_tflops, "mode_overhead_pct": overhead,
         "mode_overhead_pct_all": overhead_all, "sweep": sweep, "workloads": workloads,
+        "study": study,
         "peaks": peaks,
     }
     print(json.dumps(line))
