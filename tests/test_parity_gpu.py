@@ -533,10 +533,13 @@ def test_maximum_size(d, B, H):
     torch.cuda.empty_cache()
 
 
-def test_cuda_graph_capture_matches_eager():
+@pytest.mark.parametrize("fused_zero", [False, True], ids=["separate-zeroing", "delta-zeroes"])
+def test_cuda_graph_capture_matches_eager(fused_zero):
     # The calls allocate nothing and never synchronise, so a whole step (forward, delta,
     # backward with its zeroing and conversion, launched as programmatic dependents)
-    # captures into a CUDA graph; replaying it gives the eager results bit for bit.
+    # captures into a CUDA graph; replaying it gives the eager results bit for bit. With
+    # fused_zero the delta pass zeroes the dQ workspace (pfa_attn_delta_zero) and the
+    # backward call skips its zeroing pass, as pfa.backward does at d = 64.
     t = to_dev(inputs.gaussian(2, 4, 2, 384, 64, std_qkv=0.5, std_do=1.0, seed=11))
     q, k, v, do = t["q"], t["k"], t["v"], t["do"]
     o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
@@ -546,8 +549,12 @@ def test_cuda_graph_capture_matches_eager():
 
     def step():
         pfa.attn_fwd(q, k, v, o, lse, causal=True, scale=0.125, fix_mode=1, beta=2.0, eps=1e-3)
-        pfa.attn_delta(o, do, delta)
-        pfa.attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, ws, causal=True, scale=0.125)
+        if fused_zero:
+            pfa.attn_delta_zero(o, do, delta, ws)
+        else:
+            pfa.attn_delta(o, do, delta)
+        pfa.attn_bwd(q, k, v, do, lse, delta, dq, dk, dv, ws, causal=True, scale=0.125,
+                     workspace_zeroed=fused_zero)
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
