@@ -427,6 +427,37 @@ def measure_study(t, w, flush, k, peak):
                 "vs_fused_pct": 100.0 * (m / med["fused"] - 1.0)} for n, m in med.items()}
 
 
+def time_fwd_pair(t, wl, modes, flush, k):
+    """Forward time of the CTA-paired variant (FWD_PAIR_CTA: the two CTAs of a cluster share
+    every product, d = 128) and of the one-CTA fused forward, per mode, interleaved one call
+    at a time, L2 flushed before each, all enqueued before one synchronisation."""
+    import precision_flash_attention_gb300 as pfa
+    q = t["q"]
+    o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    calls = {}
+    for m in modes:
+        kw = dict(causal=wl.causal, scale=wl.alpha, fix_mode=m, beta=wl.beta, eps=wl.eps)
+        for pair in (False, True):
+            calls[(m, pair)] = (lambda kw=kw, fl=pfa.FWD_PAIR_CTA if pair else 0:
+                                pfa.attn_fwd_ex(q, t["k"], t["v"], o, lse, flags=fl, **kw))
+    for fn in calls.values():
+        for _ in range(2):
+            flush.fill_(1.0)
+            fn()
+    rec = {c: [] for c in calls}
+    for _ in range(k):
+        for c, fn in calls.items():
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            rec[c].append((e0, e1))
+    torch.cuda.synchronize()
+    med = {c: statistics.median(a.elapsed_time(b) for a, b in v) for c, v in rec.items()}
+    return {m: {"one": med[(m, False)], "pair": med[(m, True)]} for m in modes}
+
+
 # The other configured workloads, each timed in every mode it lists (tests check them against
 # the oracle; here they are measured). Mode 2 is added for the GPT-2 layer.
 OTHER_WORKLOADS = [
@@ -457,6 +488,7 @@ def measure_workload(name, device, steps, flush, peaks):
                    delta_mode=1 if name == "sink" else 0) for m in modes}
     splits = {m: time_step(sts[m], steps, 2, flush, split=True) for m in modes}
     step_ms_all = interleaved_step_ms(sts, steps, flush)
+    pair = time_fwd_pair(t, wl, modes, flush, steps) if d == 128 else None
     for m in modes:
         r = splits[m]
         med = {k: statistics.median(v) for k, v in r.items()}
@@ -476,6 +508,11 @@ def measure_workload(name, device, steps, flush, peaks):
         for k in ("det", "split"):
             e[f"bwd_{k}_ms"] = med[f"bwd_{k}_ms"]
             e[f"bwd_{k}_tflops"] = f_bwd / med[f"bwd_{k}_ms"] / 1e9
+        if pair is not None:
+            # The CTA-paired forward against the one-CTA forward timed beside it.
+            e["fwd_pair_ms"] = pair[m]["pair"]
+            e["fwd_pair_tflops"] = f_fwd / pair[m]["pair"] / 1e9
+            e["fwd_pair_vs_one_cta_pct"] = 100.0 * (pair[m]["pair"] / pair[m]["one"] - 1.0)
         if name != "sink":
             e["delta_ms"] = med["delta_ms"]
             e["delta_gbs"] = dl_bytes / med["delta_ms"] / 1e6
@@ -632,6 +669,21 @@ def run_gpu_arm(args):
     peaks = load_peaks()
     t = make_inputs(dev, w["B"], w["H"], w["N"], w["d"], seed=rank)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.fwd_pair:
+        # Profiling run: the forward alone, the one-CTA and the CTA-paired kernel
+        # alternating (warm-up calls included), L2 flushed before each; prints nothing.
+        if w["d"] != 128:
+            raise SystemExit("--fwd-pair needs --d 128")
+        o = torch.empty_like(t["q"])
+        lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(args.warmup + args.steps):
+            for fl in (0, pfa.FWD_PAIR_CTA):
+                flush.fill_(1.0)
+                pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=w["causal"], scale=w["scale"],
+                                fix_mode=args.mode, beta=w["beta"], eps=w["eps"], flags=fl)
+        torch.cuda.synchronize()
+        assert pfa.device_error() == 0, "device error word set during the forward run"
+        return
     head = args.mode
     # Modes 0, 1 and 2 interleaved in the timed region: the headline is `head` (1 by
     # default), and the cost of each fix mode is read against mode 0 under the same load.
@@ -878,6 +930,9 @@ def main():
                     help="override the head dimension, scale 1/sqrt(d) (profiling; d = 128 runs the "
                          "query-outer dQ pass)")
     ap.add_argument("--progress", action="store_true", help="log each stage to stderr")
+    ap.add_argument("--fwd-pair", action="store_true",
+                    help="run only the forward, one-CTA and CTA-paired alternating (with --d 128; "
+                         "for ncu captures); prints nothing")
     ap.add_argument("--kernels-only", action="store_true",
                     help="launch only the timed steps (for ncu captures); prints nothing")
     ap.add_argument("--traffic-from", metavar="CSV",

@@ -146,12 +146,20 @@ typedef struct pfa_monitor {
                                         the bias behaves with fewer mantissa bits ([PK] open
                                         questions). Combine with PFA_FWD_UNFUSED_BF16_PV for the
                                         paper's profile; not with each other. */
+#define PFA_FWD_PAIR_CTA 8u          /* d = 128, the fused path (no monitor, no study flag):
+                                        the two CTAs of a thread-block cluster share every
+                                        tensor-core product (tcgen05 cta_group::2, M = 256),
+                                        each holding half of each K and V tile, so that a
+                                        CTA's K / V loads and shared-memory operand reads
+                                        halve. Same outputs and counters as without it, up to
+                                        the FP32 summation order of the products. */
 
 /* pfa_attn_fwd with the monitor and options (no counterpart in the paper).
  * counters and monitor are optional (NULL); flags 0 and monitor NULL is
- * pfa_attn_fwd exactly. The study flags with d != 64 return PFA_ERR_UNSUPPORTED;
- * unknown flag bits, or both narrow formats, PFA_ERR_INVALID_ARG. eps must be
- * finite and >= 0 when a monitor is given. */
+ * pfa_attn_fwd exactly. The study flags with d != 64, and PFA_FWD_PAIR_CTA with
+ * d != 128, a monitor or a study flag, return PFA_ERR_UNSUPPORTED; unknown flag
+ * bits, or both narrow formats, PFA_ERR_INVALID_ARG. eps must be finite and >= 0
+ * when a monitor is given. */
 int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa_bf16* o, float* lse,
                     int B, int H_q, int H_kv, int N, int d, int causal, float scale, int fix_mode,
                     float beta, float eps, pfa_counters* counters, pfa_monitor* monitor,

@@ -15,14 +15,15 @@ import math
 
 import torch
 
-from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, BWD_WORKSPACE_ZEROED, EXPORTS, FWD_PBAR_E4M3, FWD_PBAR_MXFP4,
-                   FWD_UNFUSED_BF16_PV, MONITOR_WORDS,
+from ._lib import (BWD_DQ_DETERMINISTIC, BWD_DQ_SPLIT, BWD_WORKSPACE_ZEROED, EXPORTS, FWD_PAIR_CTA, FWD_PBAR_E4M3,
+                   FWD_PBAR_MXFP4, FWD_UNFUSED_BF16_PV, MONITOR_WORDS,
                    TIE_BINS, PfaError, attn_bwd, attn_bwd_accum, attn_bwd_ex, attn_bwd_noalloc,
                    attn_delta, attn_delta_alt, attn_delta_zero, attn_fwd, attn_fwd_ex, bwd_workspace_bytes,
                    device_error, device_error_site, load, status_string, wait_probe)
 
 __all__ = [
-    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "BWD_WORKSPACE_ZEROED", "EXPORTS", "FWD_PBAR_E4M3", "FWD_PBAR_MXFP4",
+    "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "BWD_WORKSPACE_ZEROED", "EXPORTS", "FWD_PAIR_CTA", "FWD_PBAR_E4M3",
+    "FWD_PBAR_MXFP4",
     "FWD_UNFUSED_BF16_PV", "MONITOR_WORDS",
     "TIE_BINS", "PfaError", "attn_fwd", "attn_fwd_ex", "attn_delta", "attn_delta_zero",
     "attn_delta_alt", "attn_bwd", "attn_bwd_accum", "attn_bwd_ex", "attn_bwd_noalloc",
@@ -47,14 +48,14 @@ PBAR_FLAGS = {"bf16": 0, "e4m3": FWD_PBAR_E4M3, "mxfp4": FWD_PBAR_MXFP4}
 
 
 def forward(q, k, v, *, causal=False, scale=None, fix_mode=0, beta=2.0, eps=1e-3, counters=None,
-            monitor=None, unfused_bf16_pv=False, pbar="bf16", stream=None):
+            monitor=None, unfused_bf16_pv=False, pbar="bf16", pair_cta=False, stream=None):
     """Allocate O and lse and run the forward pass (pfa_attn_fwd, or pfa_attn_fwd_ex with a
-    monitor, the unfused BF16 study profile or a narrower Pbar format: ``pbar`` "e4m3" or
-    "mxfp4"). Returns (o, lse)."""
+    monitor, the unfused BF16 study profile, a narrower Pbar format: ``pbar`` "e4m3" or
+    "mxfp4", or ``pair_cta``: at d = 128 two CTAs share each product). Returns (o, lse)."""
     scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    flags = (FWD_UNFUSED_BF16_PV if unfused_bf16_pv else 0) | PBAR_FLAGS[pbar]
+    flags = (FWD_UNFUSED_BF16_PV if unfused_bf16_pv else 0) | PBAR_FLAGS[pbar] | (FWD_PAIR_CTA if pair_cta else 0)
     if monitor is None and not flags:
         attn_fwd(q, k, v, o, lse, causal=causal, scale=scale, fix_mode=fix_mode, beta=beta, eps=eps,
                  counters=counters, stream=stream)

@@ -21,6 +21,7 @@ PFA_OK = 0
 FWD_UNFUSED_BF16_PV = 1
 FWD_PBAR_E4M3 = 2
 FWD_PBAR_MXFP4 = 4
+FWD_PAIR_CTA = 8
 TIE_BINS = 8
 MONITOR_WORDS = 1 + TIE_BINS
 # pfa_attn_bwd_ex flags (include/pfa.h)
@@ -194,7 +195,8 @@ def attn_fwd_ex(q, k, v, o, lse, *, causal: bool, scale: float, fix_mode: int = 
                 beta: float = 2.0, eps: float = 1e-3, counters=None, monitor=None, flags: int = 0,
                 stream=None) -> None:
     """pfa_attn_fwd_ex: pfa_attn_fwd with the monitor (int64[9]: operational ones, then the
-    8-bin tie-multiplicity histogram) and options (FWD_UNFUSED_BF16_PV)."""
+    8-bin tie-multiplicity histogram) and options (FWD_UNFUSED_BF16_PV, FWD_PBAR_E4M3,
+    FWD_PBAR_MXFP4, FWD_PAIR_CTA)."""
     also = []
     for t, n, words in ((counters, "counters", 3), (monitor, "monitor", MONITOR_WORDS)):
         if t is not None:

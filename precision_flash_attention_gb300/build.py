@@ -23,8 +23,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpfa.so")
 STAMP = os.path.join(BUILD_DIR, "stamp.txt")
 
-SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_fwd_study.cu", "attn_fwd_lowp.cu", "attn_bwd.cu",
-           "attn_dq.cu", "attn_delta.cu", "attn_bwd_noalloc.cu", "wait_probe.cu"]
+SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_fwd_study.cu", "attn_fwd_lowp.cu", "attn_fwd_pair.cu",
+           "attn_bwd.cu", "attn_dq.cu", "attn_delta.cu", "attn_bwd_noalloc.cu", "wait_probe.cu"]
 HEADERS = [os.path.join(CSRC, "pfa_device.cuh"), os.path.join(CSRC, "pfa_internal.h"),
            os.path.join(CSRC, "attn_fwd.cuh"), os.path.join(INCLUDE, "pfa.h")]
 

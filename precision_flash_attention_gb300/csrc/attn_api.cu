@@ -223,12 +223,15 @@ int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa
   if (!q || !k || !v || !o || !lse) return PFA_ERR_INVALID_ARG;
   int rc = check_sizes(B, H_q, H_kv, N, d);
   if (rc != PFA_OK) return rc;
-  if (flags & ~static_cast<unsigned>(PFA_FWD_UNFUSED_BF16_PV | PFA_FWD_PBAR_E4M3 | PFA_FWD_PBAR_MXFP4))
+  if (flags & ~static_cast<unsigned>(PFA_FWD_UNFUSED_BF16_PV | PFA_FWD_PBAR_E4M3 | PFA_FWD_PBAR_MXFP4 |
+                                     PFA_FWD_PAIR_CTA))
     return PFA_ERR_INVALID_ARG;
   if ((flags & PFA_FWD_PBAR_E4M3) && (flags & PFA_FWD_PBAR_MXFP4)) return PFA_ERR_INVALID_ARG;
   const bool profile = (flags & PFA_FWD_UNFUSED_BF16_PV) != 0;
   const int pbar = (flags & PFA_FWD_PBAR_E4M3) ? 1 : (flags & PFA_FWD_PBAR_MXFP4) ? 2 : 0;
+  const bool pair = (flags & PFA_FWD_PAIR_CTA) != 0;
   if ((profile || pbar) && d != 64) return PFA_ERR_UNSUPPORTED;
+  if (pair && (d != 128 || profile || pbar || monitor)) return PFA_ERR_UNSUPPORTED;
   if (!good_scale(scale) || fix_mode < 0 || fix_mode > 2) return PFA_ERR_INVALID_ARG;
   if (fix_mode == 1 && !(std::isfinite(beta) && beta > 1.f)) return PFA_ERR_INVALID_ARG;
   const bool ties = fix_mode != 0 || counters != nullptr || monitor != nullptr;
@@ -258,6 +261,12 @@ int pfa_attn_fwd_ex(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, pfa
   a.profile = profile ? 1 : 0;
   a.pbar = pbar;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (pair) {
+    // Each CTA of a pair loads half of a K tile: 64-row boxes.
+    CUtensorMap tk64;
+    if ((rc = tile_map(&tk64, k, B * H_kv, N, d, 64)) != PFA_OK) return rc;
+    return launched(pfa::launch_fwd_pair(tq, tk64, tv, a, st));
+  }
   if (pbar) return launched(pfa::launch_fwd_lowp(tq, tk, tv, a, st));
   if (profile || monitor) return launched(pfa::launch_fwd_study(tq, tk, tv, a, st));
   return launched(pfa::launch_fwd(tq, tk, tv, a, st));

@@ -74,11 +74,15 @@ constexpr int kTieBins = 8;            // tie multiplicity 1..7 and >= 8
 // Formats of the Pbar operand of the Pbar V product.
 constexpr int kPbarBf16 = 0, kPbarE4m3 = 1, kPbarMxfp4 = 2;
 
-template <int D, bool PROFILE>
+// PAIR: the two CTAs of a cluster share each product (cta_group::2, M = 256):
+// each CTA holds its own two query tiles, half of each K tile (64 keys, all d
+// columns) and half of each V tile (all keys, 64 of the d columns).
+template <int D, bool PROFILE, bool PAIR = false>
 struct FwdLayout {
   static_assert(!PROFILE || D == 64, "the unfused profile is built for d = 64");
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;   // Q pairs in flight
+  static_assert(!PAIR || (D == 128 && !PROFILE), "the CTA pairing is built for the fused d = 128 path");
+  static constexpr int kStages = (D == 64 || PAIR) ? 3 : 2;
+  static constexpr int kQBufs = (D == 64 || PAIR) ? 2 : 1;   // Q pairs in flight
   // d = 64: Pbar_t gets its own TMEM columns [384 + 64 t, 448 + 64 t), so the
   // next S_t can be computed as soon as the softmax holds the current one in
   // registers. d = 128 has no columns left and writes Pbar_t over S_t, and so
@@ -88,10 +92,14 @@ struct FwdLayout {
   static constexpr uint32_t kColU = 384;
   static constexpr int kTileBytes = kTile * D * 2;   // 128 rows x D bf16
   static constexpr int kPanelBytes = kTile * 128;    // 128 rows x 64 bf16
+  static constexpr int kKRows = PAIR ? kTile / 2 : kTile;          // keys of a K stage
+  static constexpr int kKPanelBytes = kKRows * 128;                 // kKRows x 64 bf16
+  static constexpr int kKBytes = kKRows * D * 2;                    // one K stage
+  static constexpr int kVBytes = PAIR ? kPanelBytes : kTileBytes;   // one V stage
   static constexpr int kQ = 0;                       // + (buffer * 2 + t) * tile
-  static constexpr int kK = kQBufs * 2 * kTileBytes; // + stage * tile
-  static constexpr int kV = kK + kStages * kTileBytes;
-  static constexpr int kBars = kV + kStages * kTileBytes;
+  static constexpr int kK = kQBufs * 2 * kTileBytes; // + stage * kKBytes
+  static constexpr int kV = kK + kStages * kKBytes;  // + stage * kVBytes
+  static constexpr int kBars = kV + kStages * kVBytes;
   static constexpr int bQFull = 0;                    // + Q buffer
   static constexpr int bQEmpty = bQFull + kQBufs;     // + Q buffer: the item's products are done
   static constexpr int bKVFull = bQEmpty + kQBufs;    // + stage
@@ -110,11 +118,12 @@ struct FwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE, int PBAR = kPbarBf16>
+template <int D, int MODE, bool CAUSAL, int MON, bool PROFILE, int PBAR = kPbarBf16, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdArgs args) {
-  using L = FwdLayout<D, PROFILE>;
+  using L = FwdLayout<D, PROFILE, PAIR>;
+  static_assert(!PAIR || (MON <= 1 && PBAR == kPbarBf16), "the CTA pairing is built for the fused path");
   constexpr bool kCount = MON >= 1;
   constexpr bool kMonitor = MON >= 2;
   // The repetition flag is needed by the fix modes and by the repeated-row
@@ -125,35 +134,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   PFA_TRACE_DECL();
+  // PAIR: the cluster's two CTAs work on one item; the even one (the leader)
+  // issues every product of the pair.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
 
   const AttnShape& sh = args.s;
   const int N = sh.N;
   const int n_kt = (N + kTile - 1) / kTile;   // key tiles == query tiles
-  const int n_pairs = (n_kt + 1) / 2;
+  // An item is two query tiles of one CTA, or, paired, four: the even CTA's
+  // tiles 4g, 4g + 2 and the odd CTA's 4g + 1, 4g + 3 (t = 0 pairs 4g with 4g + 1).
+  constexpr int kGroup = PAIR ? 4 : 2;
+  const int n_groups = (n_kt + kGroup - 1) / kGroup;
   const int BHq = sh.B * sh.Hq;
-  const int n_items = n_pairs * BHq;
-  const int item0 = static_cast<int>(blockIdx.x);
-  const int stride = static_cast<int>(gridDim.x);
-  // The k-th item of this CTA: rounds of gridDim.x items, taken left to right in
-  // even rounds and right to left in odd ones, so that a CTA given a heavy item
-  // early gets a light one in the next round.
+  const int n_items = n_groups * BHq;
+  const int item0 = static_cast<int>(PAIR ? blockIdx.x >> 1 : blockIdx.x);
+  const int stride = static_cast<int>(PAIR ? gridDim.x >> 1 : gridDim.x);
+  // The k-th item of this CTA (cluster): rounds of `stride` items, taken left to
+  // right in even rounds and right to left in odd ones, so that a CTA given a
+  // heavy item early gets a light one in the next round.
   auto item_at = [&](int k) { return k * stride + ((k & 1) ? stride - 1 - item0 : item0); };
-  // Work item -> (pair of query tiles, batch and query head); pairs heaviest first.
+  // Work item -> (query tiles, batch and query head); heaviest groups first.
   struct Item {
-    int bh, bh_kv, qt0, last0, last1, n_iter;
+    int bh, bh_kv, qt0, qt1, last0, last1, n_iter;
     bool has1;
   };
   auto decode = [&](int item) {
     Item it;
     it.bh = item % BHq;
-    const int pair = n_pairs - 1 - item / BHq;
+    const int grp = n_groups - 1 - item / BHq;
     const int b = it.bh / sh.Hq, h = it.bh % sh.Hq;
     it.bh_kv = b * sh.Hkv + h / (sh.Hq / sh.Hkv);
-    it.qt0 = 2 * pair;
-    it.has1 = it.qt0 + 1 < n_kt;
-    // Last key tile each query tile visits (-1: the tile does not exist).
-    it.last0 = CAUSAL ? it.qt0 : n_kt - 1;
-    it.last1 = it.has1 ? (CAUSAL ? it.qt0 + 1 : n_kt - 1) : -1;
+    if constexpr (PAIR) {
+      // Both CTAs visit the key tiles of the later tile of each product; the
+      // earlier tile's rows see the extra diagonal tile fully masked. A tile past
+      // the end is loaded as zeros and stores nothing.
+      const int base = 4 * grp;
+      it.qt0 = base + static_cast<int>(rank);
+      it.qt1 = base + 2 + static_cast<int>(rank);
+      it.has1 = base + 2 < n_kt;
+      it.last0 = CAUSAL ? min(base + 1, n_kt - 1) : n_kt - 1;
+      it.last1 = it.has1 ? (CAUSAL ? min(base + 3, n_kt - 1) : n_kt - 1) : -1;
+    } else {
+      it.qt0 = 2 * grp;
+      it.qt1 = it.qt0 + 1;
+      it.has1 = it.qt1 < n_kt;
+      // Last key tile each query tile visits (-1: the tile does not exist).
+      it.last0 = CAUSAL ? it.qt0 : n_kt - 1;
+      it.last1 = it.has1 ? (CAUSAL ? it.qt1 : n_kt - 1) : -1;
+    }
     it.n_iter = max(it.last0, it.last1) + 1;
     return it;
   };
@@ -163,20 +192,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) { return sbase + L::kBars + 8u * static_cast<uint32_t>(i); };
   const WaitCtl ctl{abort_flag, args.err, args.err_site, sbase, 1u};
 
+  // PAIR: the leader's Q and K / V barriers complete on its own copies and on one
+  // arrival from the odd CTA's warp 1, which forwards the completion of the odd
+  // CTA's copies; the leader's PFull_t counts the softmax warps of both CTAs.
+  const uint32_t n_full = PAIR && leader ? 2u : 1u;
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
     if (sbase & 1023u) atomicOr(args.err, PFA_DEVERR_SMEM_ALIGN);
     for (int qb = 0; qb < L::kQBufs; ++qb) {
-      mbar_init(bar(L::bQFull + qb), 1);
+      mbar_init(bar(L::bQFull + qb), n_full);
       mbar_init(bar(L::bQEmpty + qb), 1);
     }
     for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::bKVFull + s), 1);
+      mbar_init(bar(L::bKVFull + s), n_full);
       mbar_init(bar(L::bKVEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(L::bSFull + t), 1);
-      mbar_init(bar(L::bPFull + t), 4);
+      mbar_init(bar(L::bPFull + t), PAIR ? 8 : 4);
       mbar_init(bar(L::bODone + t), 1);
       mbar_init(bar(L::bSFree + t), 4);
       mbar_init(bar(L::bPVDone + t), 1);
@@ -186,11 +219,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  // PAIR: neither CTA's barriers are signalled by the other before both are set up.
+  if constexpr (PAIR) cluster_sync_all();
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // Setup done: let the next kernel on the stream be scheduled as CTAs leave, and
@@ -216,12 +256,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < it.n_iter; ++j, ++gk) {
           const int s = gk % L::kStages;
           if (!(ok = wait_warp(bar(L::bKVEmpty + s), ((gk / L::kStages) & 1) ^ 1, ctl))) break;
-          mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), 2 * L::kTileBytes);
-          for (int p = 0; p < D / 64; ++p) {
-            tma_load_3d_warp(sbase + L::kK + s * L::kTileBytes + p * L::kPanelBytes, &tmK,
-                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
-            tma_load_3d_warp(sbase + L::kV + s * L::kTileBytes + p * L::kPanelBytes, &tmV,
-                             bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
+          mbar_arrive_expect_tx_warp(bar(L::bKVFull + s), L::kKBytes + L::kVBytes);
+          if constexpr (PAIR) {
+            // This CTA's half: keys 64 rank .. 64 rank + 63 of K (a map with
+            // 64-row boxes), columns 64 rank .. 64 rank + 63 of V.
+            for (int p = 0; p < D / 64; ++p)
+              tma_load_3d_warp(sbase + L::kK + s * L::kKBytes + p * L::kKPanelBytes, &tmK,
+                               bar(L::bKVFull + s), p * 64, j * kTile + 64 * static_cast<int>(rank), it.bh_kv);
+            tma_load_3d_warp(sbase + L::kV + s * L::kVBytes, &tmV, bar(L::bKVFull + s),
+                             64 * static_cast<int>(rank), j * kTile, it.bh_kv);
+          } else {
+            for (int p = 0; p < D / 64; ++p) {
+              tma_load_3d_warp(sbase + L::kK + s * L::kKBytes + p * L::kKPanelBytes, &tmK,
+                               bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
+              tma_load_3d_warp(sbase + L::kV + s * L::kVBytes + p * L::kPanelBytes, &tmV,
+                               bar(L::bKVFull + s), p * 64, j * kTile, it.bh_kv);
+            }
           }
         }
       }
@@ -237,48 +287,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode(item);
         const int qb = ti % L::kQBufs;
         if (!(ok = wait_warp(bar(L::bQEmpty + qb), ((ti / L::kQBufs) & 1) ^ 1, ctl))) break;
-        mbar_arrive_expect_tx_warp(bar(L::bQFull + qb), (it.has1 ? 2 : 1) * L::kTileBytes);
-        for (int t = 0; t < (it.has1 ? 2 : 1); ++t)
+        // PAIR: a product reads the tile of both CTAs, so both are always loaded
+        // (zeros past the end).
+        const int n_t = (PAIR || it.has1) ? 2 : 1;
+        mbar_arrive_expect_tx_warp(bar(L::bQFull + qb), n_t * L::kTileBytes);
+        for (int t = 0; t < n_t; ++t)
           for (int p = 0; p < D / 64; ++p)
             tma_load_3d_warp(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + p * L::kPanelBytes, &tmQ,
-                             bar(L::bQFull + qb), p * 64, (it.qt0 + t) * kTile, it.bh);
+                             bar(L::bQFull + qb), p * 64, (t ? it.qt1 : it.qt0) * kTile, it.bh);
         // With one Q buffer the next pair waits for this item: start it into L2.
         if (L::kQBufs == 1 && item_at(k + 1) < n_items) {
           const Item nx = decode(item_at(k + 1));
           for (int t = 0; t < (nx.has1 ? 2 : 1); ++t)
-            for (int p = 0; p < D / 64; ++p) tma_prefetch_l2_3d_warp(&tmQ, p * 64, (nx.qt0 + t) * kTile, nx.bh);
+            for (int p = 0; p < D / 64; ++p)
+              tma_prefetch_l2_3d_warp(&tmQ, p * 64, (t ? nx.qt1 : nx.qt0) * kTile, nx.bh);
         }
       }
       for (int i = ti > L::kQBufs ? ti - L::kQBufs : 0; i < ti; ++i)
         wait_drain(bar(L::bQFull + i % L::kQBufs), (i / L::kQBufs) & 1, ctl);
       (void)ok;
+    } else if (warp == 1 && PAIR && !leader) {
+      // ---------------- relay (odd CTA of a pair) ----------------
+      // Forwards the completion of this CTA's Q and K / V copies to the leader's
+      // barriers, in the order in which the leader consumes them.
+      int gk = 0, ti = 0;
+      bool ok = true;
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++ti) {
+        const Item it = decode(item);
+        const int qb = ti % L::kQBufs;
+        if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(L::bQFull + qb), 0));
+        for (int j = 0; ok && j < it.n_iter; ++j) {
+          const int s = (gk + j) % L::kStages;
+          if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(L::bKVFull + s), 0));
+        }
+        gk += it.n_iter;
+      }
     } else if (warp == 1) {
       // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
-      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idPV = idesc_bf16(128, D, false, true);
+      // PAIR: M = 256 over the pair's two tiles t; each CTA supplies half of the
+      // B operand (K: 64 keys; V: 64 of the d columns) and holds its 128 rows of
+      // S_t and Obar_t in its own TMEM. Every commit arrives in both CTAs.
+      constexpr int kM = PAIR ? 256 : 128;
+      constexpr uint32_t idS = idesc_bf16(kM, 128, false, false);
+      constexpr uint32_t idPV = idesc_bf16(kM, D, false, true);
+      auto commit = [&](uint32_t b) {
+        if constexpr (PAIR) umma_pair_commit_mc_warp(b, 3);
+        else umma_commit_warp(b);
+      };
       // S_t = Q_t K_j^T from Q buffer qb and K/V stage s.
       auto issue_s = [&](int t, int qb, int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
-          umma_bf16_warp(tmem + 128 * t,
-                         sdesc_sw128(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + koff, 16, 1024),
-                         sdesc_sw128(sbase + L::kK + s * L::kTileBytes + koff, 16, 1024), idS, kk > 0);
+          const uint32_t qoff = (kk >> 2) * L::kPanelBytes + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * L::kKPanelBytes + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(sbase + L::kQ + (qb * 2 + t) * L::kTileBytes + qoff, 16, 1024);
+          const uint64_t b = sdesc_sw128(sbase + L::kK + s * L::kKBytes + koff, 16, 1024);
+          if constexpr (PAIR) umma_pair_bf16_warp(tmem + 128 * t, a, b, idS, kk > 0);
+          else umma_bf16_warp(tmem + 128 * t, a, b, idS, kk > 0);
         }
-        umma_commit_warp(bar(L::bSFull + t));
+        commit(bar(L::bSFull + t));
       };
       // Obar_t (+)= Pbar_t V_j; Pbar_t is 64 BF16-pair columns (its own with the
       // split layout, else the first 64 of S_t), 8 columns per K step.
-      // The profile's product of each key tile starts afresh in U_t.
+      // The profile's product of each key tile starts afresh in U_t. PAIR: this
+      // CTA's V half is one 64-column block, so the block stride is not used (0
+      // keeps every address inside that block).
       auto issue_pv = [&](int t, int s, int j) {
         const uint32_t tp = tmem + (L::kSplitP ? L::kColP + 64u * t : 128u * t);
         const uint32_t td = tmem + (PROFILE ? L::kColU + 64u * t : 256u + D * t);
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk)
-          umma_bf16_tmem_a_warp(td, tp + 8 * kk,
-                                sdesc_sw128(sbase + L::kV + s * L::kTileBytes + kk * 2048,
-                                            L::kPanelBytes, 1024),
-                                idPV, ((!PROFILE && j > 0) || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(sbase + L::kV + s * L::kVBytes + kk * 2048, PAIR ? 0u : L::kPanelBytes, 1024);
+          const uint32_t acc = ((!PROFILE && j > 0) || kk > 0) ? 1u : 0u;
+          if constexpr (PAIR) umma_pair_bf16_tmem_a_warp(td, tp + 8 * kk, b, idPV, acc);
+          else umma_bf16_tmem_a_warp(td, tp + 8 * kk, b, idPV, acc);
+        }
       };
       // Phases across items: gk key tiles so far (the K/V ring), c_t scores of
       // tile t so far (SFull_t and PFull_t), ti items (the Q buffers).
@@ -293,11 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const Item it = decode(item);
           const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
           const int qb = ti % L::kQBufs;
-          if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
+          if (!(ok = wait_warp<PAIR>(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
           for (int j = 0; ok && j <= n_iter; ++j) {
             if (j < n_iter) {
               const int s = (gk + j) % L::kStages;
-              if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
+              if (!(ok = wait_warp<PAIR>(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
               if (lane == 0) PFA_FWD_TRACE(0, 1, j);
               if (j <= last0) {
                 if (c0 + j > 0 && !(ok = wait_warp(bar(L::bSFree + 0), (c0 + j - 1) & 1, ctl))) break;
@@ -314,26 +399,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int jp = j - 1;
               const int sp = (gk + jp) % L::kStages;
               if (jp <= last0) {
-                if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + jp) & 1, ctl))) break;
+                if (!(ok = wait_warp<PAIR>(bar(L::bPFull + 0), (c0 + jp) & 1, ctl))) break;
                 if (lane == 0) PFA_FWD_TRACE(0, 3, jp);
                 tc_fence_after();
                 issue_pv(0, sp, jp);
-                umma_commit_warp(bar(L::bPVDone + 0));
-                if (jp == last0) umma_commit_warp(bar(L::bODone + 0));
+                commit(bar(L::bPVDone + 0));
+                if (jp == last0) commit(bar(L::bODone + 0));
               }
               if (jp <= last1) {
-                if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + jp) & 1, ctl))) break;
+                if (!(ok = wait_warp<PAIR>(bar(L::bPFull + 1), (c1 + jp) & 1, ctl))) break;
                 if (lane == 0) PFA_FWD_TRACE(0, 2, jp);
                 tc_fence_after();
                 issue_pv(1, sp, jp);
-                umma_commit_warp(bar(L::bPVDone + 1));
-                if (jp == last1) umma_commit_warp(bar(L::bODone + 1));
+                commit(bar(L::bPVDone + 1));
+                if (jp == last1) commit(bar(L::bODone + 1));
               }
-              umma_commit_warp(bar(L::bKVEmpty + sp));
+              commit(bar(L::bKVEmpty + sp));
             }
           }
           // The item's products are done once this arrives: its Q buffer is free.
-          umma_commit_warp(bar(L::bQEmpty + qb));
+          commit(bar(L::bQEmpty + qb));
           gk += n_iter;
           c0 += last0 + 1;
           c1 += last1 + 1;
@@ -343,51 +428,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode(item);
         const int last0 = it.last0, last1 = it.last1, n_iter = it.n_iter;
         const int qb = ti % L::kQBufs;
-        if (!(ok = wait_warp(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
+        if (!(ok = wait_warp<PAIR>(bar(L::bQFull + qb), (ti / L::kQBufs) & 1, ctl))) break;
         for (int j = 0; ok && j < n_iter; ++j) {
           const int s = (gk + j) % L::kStages;
-          if (!(ok = wait_warp(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
+          if (!(ok = wait_warp<PAIR>(bar(L::bKVFull + s), ((gk + j) / L::kStages) & 1, ctl))) break;
           const bool act0 = j <= last0, act1 = j <= last1;
           if (lane == 0) PFA_FWD_TRACE(0, 1, j);
           tc_fence_after();
           if (act0) issue_s(0, qb, s);
           if (j > 0 && j - 1 <= last1) {
-            if (!(ok = wait_warp(bar(L::bPFull + 1), (c1 + j - 1) & 1, ctl))) break;
+            if (!(ok = wait_warp<PAIR>(bar(L::bPFull + 1), (c1 + j - 1) & 1, ctl))) break;
             if (lane == 0) PFA_FWD_TRACE(0, 2, j - 1);
             tc_fence_after();
             const int sp = (gk + j - 1) % L::kStages;
             issue_pv(1, sp, j - 1);
-            umma_commit_warp(bar(L::bKVEmpty + sp));
-            if (j - 1 == last1) umma_commit_warp(bar(L::bODone + 1));
+            commit(bar(L::bKVEmpty + sp));
+            if (j - 1 == last1) commit(bar(L::bODone + 1));
           }
           if (act1) issue_s(1, qb, s);
           if (act0) {
-            if (!(ok = wait_warp(bar(L::bPFull + 0), (c0 + j) & 1, ctl))) break;
+            if (!(ok = wait_warp<PAIR>(bar(L::bPFull + 0), (c0 + j) & 1, ctl))) break;
             if (lane == 0) PFA_FWD_TRACE(0, 3, j);
             tc_fence_after();
             issue_pv(0, s, j);
-            if (j == last0) umma_commit_warp(bar(L::bODone + 0));
-            if (!act1) umma_commit_warp(bar(L::bKVEmpty + s));
+            if (j == last0) commit(bar(L::bODone + 0));
+            if (!act1) commit(bar(L::bKVEmpty + s));
           }
         }
         if (ok && last1 == n_iter - 1) {
           const int j = n_iter - 1;
-          if ((ok = wait_warp(bar(L::bPFull + 1), (c1 + j) & 1, ctl))) {
+          if ((ok = wait_warp<PAIR>(bar(L::bPFull + 1), (c1 + j) & 1, ctl))) {
             tc_fence_after();
             issue_pv(1, (gk + j) % L::kStages, j);
-            umma_commit_warp(bar(L::bKVEmpty + (gk + j) % L::kStages));
-            umma_commit_warp(bar(L::bODone + 1));
+            commit(bar(L::bKVEmpty + (gk + j) % L::kStages));
+            commit(bar(L::bODone + 1));
           }
         }
         // The item's products are done once this arrives: its Q buffer is free.
-        umma_commit_warp(bar(L::bQEmpty + qb));
+        commit(bar(L::bQEmpty + qb));
         gk += n_iter;
         c0 += last0 + 1;
         c1 += last1 + 1;
       }
       }
       // Drain: no MMA may still read shared memory or write TMEM at teardown.
-      umma_commit_warp(bar(L::bDrain));
+      if constexpr (PAIR) umma_pair_commit_warp(bar(L::bDrain));
+      else umma_commit_warp(bar(L::bDrain));
       wait_drain(bar(L::bDrain), 0, ctl);
     }
     }
@@ -453,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int last = t ? itm.last1 : itm.last0;
       if (last < 0) continue;             // the pair has no second tile
       const int bh = itm.bh;
-      const int q0 = (itm.qt0 + t) * kTile;
+      const int q0 = (t ? itm.qt1 : itm.qt0) * kTile;
       const int qrow = q0 + r;
       const bool row_ok = qrow < N;
       float m1 = -INFINITY;                  // running maximum of raw scores
@@ -681,7 +767,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 7, j);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(bar(L::bPFull + t));
+        if (lane == 0 && ok) {
+          // PAIR: the leader's PFull_t, which counts both CTAs' softmax warps.
+          if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar(L::bPFull + t), 0));
+          else mbar_arrive(bar(L::bPFull + t));
+        }
 
         if (lane == 0 && quarter == 0) PFA_FWD_TRACE(1 + t, 8, j);
         if (!ok) break;
@@ -770,10 +860,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA frees its TMEM or leaves while the leader's products or
+  // the other CTA's arrivals may still reach it.
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+    else tmem_dealloc(tmem, 512);
   }
 }
 
@@ -792,6 +886,43 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   const long long n_items = static_cast<long long>((n_kt + 1) / 2) * a.s.B * a.s.Hq;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
   return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, a);
+}
+
+// The paired fused path at d = 128: clusters of two CTAs, as many as the device
+// holds at once (at most one per item of four query tiles), launched as a
+// programmatic dependent like the others. `tk` maps K with 64-row boxes.
+template <int MODE, bool CAUSAL, int MON>
+cudaError_t launch_fwd_pair_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<128, false, true>;
+  auto kern = attn_fwd_kernel<128, MODE, CAUSAL, MON, false, kPbarBf16, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if ((e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg)) != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  const int n_kt = (a.s.N + kTile - 1) / kTile;
+  const long long n_items = static_cast<long long>((n_kt + 3) / 4) * a.s.B * a.s.Hq;
+  cfg.gridDim = dim3(2u * static_cast<unsigned>(n_items < clusters ? n_items : clusters));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, a);
 }
 
 }  // namespace fwd

@@ -100,6 +100,10 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 // BF16 profile (a.profile, d = 64); counters as in launch_fwd.
 cudaError_t launch_fwd_study(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const FwdArgs& a, cudaStream_t stream);
+// The fused path at d = 128 with two CTAs per product (cta_group::2); tk maps K
+// with 64-row boxes (tile_map rows = 64).
+cudaError_t launch_fwd_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdArgs& a, cudaStream_t stream);
 // The narrow Pbar formats (a.pbar 1 or 2; d = 64, monitor counted, profile or fused).
 cudaError_t launch_fwd_lowp(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdArgs& a, cudaStream_t stream);

@@ -181,8 +181,12 @@ def test_fwd_ex_validates(lib):
         a.update(kw)
         return lib.pfa_attn_fwd_ex(*a.values())
 
-    assert call(flags=8) == inv                       # an unknown flag bit
+    assert call(flags=16) == inv                      # an unknown flag bit
     assert call(flags=2 | 4) == inv                   # both narrow Pbar formats at once
+    # The CTA pairing is built for the fused d = 128 path only.
+    assert call(flags=8) == -3
+    assert call(flags=8, d=128, monitor=A) == -3
+    assert call(flags=8 | 2, d=128) == -3
     assert call(monitor=A + 4) == mis                 # the monitor must be 8-byte aligned
     assert call(monitor=A, eps=-1.0) == inv           # the monitor needs a valid eps
     assert call(q=None) == inv
