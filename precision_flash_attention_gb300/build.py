@@ -26,7 +26,8 @@ STAMP = os.path.join(BUILD_DIR, "stamp.txt")
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_fwd_study.cu", "attn_fwd_lowp.cu", "attn_fwd_pair.cu",
            "attn_bwd.cu", "attn_dq.cu", "attn_delta.cu", "attn_bwd_noalloc.cu", "wait_probe.cu"]
 HEADERS = [os.path.join(CSRC, "pfa_device.cuh"), os.path.join(CSRC, "pfa_internal.h"),
-           os.path.join(CSRC, "attn_fwd.cuh"), os.path.join(INCLUDE, "pfa.h")]
+           os.path.join(CSRC, "attn_fwd.cuh"), os.path.join(CSRC, "pfa_trace.cuh"),
+           os.path.join(INCLUDE, "pfa.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -82,12 +83,30 @@ def _product_text(path: str) -> bytes:
     return "\n".join(t.strip() for t in text.splitlines() if t.strip()).encode()
 
 
+def _local_includes(path: str, seen: list) -> list:
+    """`path` and, depth first, the project headers it includes (#include "..."), each once."""
+    if path in seen:
+        return seen
+    seen.append(path)
+    with open(path, encoding="utf-8") as f:
+        for name in re.findall(r'^\s*#include\s+"([^"]+)"', f.read(), flags=re.M):
+            for d in (CSRC, INCLUDE):
+                cand = os.path.join(d, name)
+                if os.path.exists(cand):
+                    _local_includes(cand, seen)
+                    break
+    return seen
+
+
 def kernel_source_digest(kernel: str) -> str:
-    """Hash of the sources one kernel is built from (see KERNEL_SOURCES), as the
-    product build compiles them."""
+    """Hash of the sources one kernel is built from (see KERNEL_SOURCES): its translation
+    unit, the API file that builds its launch arguments and the project headers the two
+    include, as the product build compiles them."""
     h = hashlib.sha256()
-    tus = [KERNEL_SOURCES[kernel], "attn_api.cu"]
-    for path in [os.path.join(CSRC, s) for s in tus] + HEADERS:
+    files = []
+    for tu in (KERNEL_SOURCES[kernel], "attn_api.cu"):
+        _local_includes(os.path.join(CSRC, tu), files)
+    for path in files:
         h.update(_product_text(path))
     return h.hexdigest()
 

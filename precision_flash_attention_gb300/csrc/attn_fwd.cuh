@@ -768,8 +768,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && ok) {
-          // PAIR: the leader's PFull_t, which counts both CTAs' softmax warps.
-          if constexpr (PAIR) mbar_arrive_cluster(mapa_shared(bar(L::bPFull + t), 0));
+          // PAIR: the leader's PFull_t, which counts both CTAs' softmax warps; only
+          // the odd CTA's arrivals need the release at cluster scope.
+          if (PAIR && !leader) mbar_arrive_cluster(mapa_shared(bar(L::bPFull + t), 0));
           else mbar_arrive(bar(L::bPFull + t));
         }
 

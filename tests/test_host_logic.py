@@ -37,6 +37,19 @@ def test_kernel_digest_is_per_kernel():
     assert build.kernel_source_digest("convert_dq_kernel") == d_bwd   # same translation unit
 
 
+def test_kernel_digest_follows_includes():
+    # A kernel's digest covers the headers its translation unit (and the API file) include,
+    # transitively, and no others: the forward kernel's header is not the backward kernel's.
+    def names(tu):
+        seen = []
+        for f in (tu, "attn_api.cu"):
+            build._local_includes(os.path.join(build.CSRC, f), seen)
+        return {os.path.basename(p) for p in seen}
+    bwd, fwd = names("attn_bwd.cu"), names("attn_fwd.cu")
+    assert {"pfa_device.cuh", "pfa_internal.h", "pfa.h"} <= bwd and "attn_fwd.cuh" not in bwd
+    assert {"attn_fwd.cuh", "pfa_device.cuh", "pfa_trace.cuh", "pfa.h"} <= fwd
+
+
 def test_reference_arm_json_line():
     # The reference arm times the float64 oracle on the host; one short step is enough here.
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],

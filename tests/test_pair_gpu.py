@@ -121,3 +121,17 @@ def test_pair_in_a_training_step():
     for a, b in zip(grads1, grads2):
         assert torch.equal(a, b)
     assert all(torch.isfinite(x.float()).all() for x in grads)
+
+
+def test_pair_flag_is_refused_where_not_built():
+    t = to_dev(inputs.gaussian(1, 1, 1, 64, 64, seed=0))
+    o = torch.empty_like(t["q"])
+    lse = torch.empty(t["q"].shape[:3], dtype=torch.float32, device="cuda")
+    with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):      # d = 64
+        pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=pfa.FWD_PAIR_CTA)
+    t = to_dev(inputs.gaussian(1, 1, 1, 64, 128, seed=0))
+    o = torch.empty_like(t["q"])
+    with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):      # with the monitor
+        pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, monitor=pfa.new_monitor(),
+                        flags=pfa.FWD_PAIR_CTA)
+    assert pfa.device_error() == 0

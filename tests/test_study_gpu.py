@@ -146,7 +146,7 @@ def test_unfused_profile_rejects_d128_and_unknown_flags():
     with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):
         pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=1)
     with pytest.raises(pfa.PfaError, match="INVALID_ARG"):
-        pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=8)
+        pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=16)
     with pytest.raises(pfa.PfaError, match="UNSUPPORTED"):
         pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, flags=2)
     assert pfa.device_error() == 0
