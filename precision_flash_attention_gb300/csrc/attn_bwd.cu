@@ -37,7 +37,6 @@
 // dP^T(i+1) and dQ(i), at d = 128 (dQ over dP^T) dQ(i) and dP^T(i+1), so the next
 // tile's scores are ready when the compute warps finish dS(i).
 #include <algorithm>
-#include <vector>
 
 #include "pfa_device.cuh"
 #include "pfa_trace.cuh"
@@ -117,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
                     const __grid_constant__ CUtensorMap tmdV, const BwdArgs args,
-                    const __grid_constant__ BwdDeal deal) {
+                    const __grid_constant__ Deal deal) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -762,13 +761,20 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // One deal per thread for the shape last launched from it.
   struct Cached {
     int key[5] = {-1, -1, -1, -1, -1};
-    BwdDeal deal;
+    Deal deal;
   };
   thread_local Cached cache;
   const int n_t = (a.s.N + kTile - 1) / kTile, bh_kv = a.s.B * a.s.Hkv, group = a.s.Hq / a.s.Hkv;
   const int key[5] = {n_t, bh_kv, group, CAUSAL ? 1 : 0, static_cast<int>(grid.x)};
   if (!std::equal(key, key + 5, cache.key)) {
-    make_bwd_deal(n_t, bh_kv, group, CAUSAL, static_cast<int>(grid.x), &cache.deal);
+    // Query tiles an item visits: from its key tile kt = item / bh_kv on (all of them
+    // without the causal mask), for each of the group's query heads. Equal items
+    // (no mask) are dealt evenly by the serpentine rounds.
+    cache.deal.rounds = 0;
+    if (CAUSAL)
+      make_deal(n_items, static_cast<int>(grid.x),
+                [](long long item, const int* p) { return p[2] * (p[0] - static_cast<int>(item / p[1])); },
+                key, &cache.deal);
     std::copy(key, key + 5, cache.key);
   }
   return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, tdo, tdq, tdk, tdv, a,
@@ -805,35 +811,6 @@ cudaError_t dispatch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }
 
 }  // namespace
-
-void make_bwd_deal(int n_t, int bh_kv, int group, bool causal, int grid, BwdDeal* out) {
-  out->rounds = 0;
-  const long long n_items = static_cast<long long>(n_t) * bh_kv;
-  if (!causal || grid < 1 || n_items >= 65535) return;   // equal items: serpentine is even
-  const int rounds = static_cast<int>((n_items + grid - 1) / grid);
-  if (static_cast<long long>(rounds) * grid > kMaxDeal) return;
-  // Query tiles an item visits: its key tile kt = item / bh_kv and every query tile
-  // from kt on, for each of the group's query heads.
-  auto size = [&](long long item) { return group * (n_t - static_cast<int>(item / bh_kv)); };
-  std::vector<long long> serp(grid, 0), load(grid, 0);
-  std::vector<int> order(grid);
-  for (int r = 0; r < rounds; ++r) {
-    for (int c = 0; c < grid; ++c) {
-      const long long it = static_cast<long long>(r) * grid + ((r & 1) ? grid - 1 - c : c);
-      if (it < n_items) serp[c] += size(it);
-    }
-    for (int c = 0; c < grid; ++c) order[c] = c;
-    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return load[x] < load[y]; });
-    for (int i = 0; i < grid; ++i) {
-      const long long it = static_cast<long long>(r) * grid + i;
-      const int c = order[i];
-      out->item[r * grid + c] = static_cast<uint16_t>(it < n_items ? it : n_items);
-      if (it < n_items) load[c] += size(it);
-    }
-  }
-  if (*std::max_element(load.begin(), load.end()) < *std::max_element(serp.begin(), serp.end()))
-    out->rounds = rounds;
-}
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,

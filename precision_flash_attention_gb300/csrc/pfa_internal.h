@@ -84,14 +84,21 @@ struct BwdArgs {
   unsigned long long* err_site;
 };
 
-// A static deal of the backward kernel's work items (key tiles, heaviest first)
+// A static deal of a persistent kernel's work items (in order, heaviest first)
 // over its CTAs: item[r * grid + c] is CTA c's item in round r (n_items where it
 // has none). rounds == 0: the kernel deals serpentine rounds itself.
 constexpr int kMaxDeal = 152 * 8;
-struct BwdDeal {
+struct Deal {
   int rounds;
   uint16_t item[kMaxDeal];
 };
+
+// Rounds of `grid` items in order; each round's items, largest first, go to the CTAs
+// with the least work so far (ties by index). `size(i)` is item i's work. Kept only
+// where its busiest CTA has less work than under the serpentine deal and the table
+// fits (n_items < 65535, rounds x grid <= kMaxDeal); otherwise out->rounds = 0.
+void make_deal(long long n_items, int grid, int (*size)(long long item, const int* p), const int* p,
+               Deal* out);
 
 struct DqArgs {
   AttnShape s;
@@ -126,11 +133,6 @@ cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const
 // 128-byte swizzle (the reduce-add target of the d = 64 kernel); tdk, tdv: BF16
 // [B*Hkv, N, d] maps of dK, dV with 64-column x 32-row boxes and 128-byte swizzle
 // (the store targets of the d = 64 kernel's drain warps).
-// The backward kernel's deal (make_bwd_deal): rounds of `grid` items in order; each
-// round's items, largest first, go to the CTAs with the least work so far (ties by
-// index). Kept only where its busiest CTA has fewer query tiles to visit than under
-// the serpentine deal and the table fits; otherwise rounds = 0.
-void make_bwd_deal(int n_t, int bh_kv, int group, bool causal, int grid, BwdDeal* out);
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);

@@ -283,6 +283,25 @@ def test_backward_dealt_from_a_table(d):
     assert_bwd_close(got, ref, f"dealt d={d}")
 
 
+def test_gpt2_shape_n2048_sampled_rows():
+    # The GPT-2 shape at N = 2048 (a point of the bench's sweep): 768 forward items over
+    # 152 CTAs, five serpentine rounds. Sampled rows of every head.
+    B, H, N = 8, 12, 2048
+    t = inputs.gaussian(B, H, H, N, 64, std_qkv=0.7, std_do=1.0, seed=21)
+    kw = dict(causal=True, scale=0.125, fix_mode=1, beta=2.0)
+    got = run_gpu(t, bwd=False, **kw)
+    rows = sampled_rows(N, 48, seed=4)
+    acc = ([], [], [], [])
+    for b in range(B):
+        for h in range(H):
+            r = oracle.attn_fwd_head(f64(t["q"][b, h]), f64(t["k"][b, h]), f64(t["v"][b, h]), rows=rows, **kw)
+            for lst, x in zip(acc, (got["o"][b, h, rows], r["o"], got["lse"][b, h, rows], r["lse"])):
+                lst.append(x)
+    cat = [np.concatenate(a) for a in acc]
+    assert_fwd_close({"o": cat[0], "lse": cat[2]}, {"o": cat[1], "lse": cat[3]}, "gpt2 N=2048")
+    assert got["counters"]["nonfinite_rows"] == 0
+
+
 def _check_groups(t, got, groups, *, causal, scale, mode, beta, dq_emulated=False,
                   delta_mode=0):
     for b, hk in groups:
