@@ -28,12 +28,13 @@ def to_dev(t: dict) -> dict:
 
 
 def run_gpu(t: dict, *, causal, scale, fix_mode, beta=2.0, eps=1e-3, bwd=True, delta_mode=0,
-            dq_mode="atomic"):
-    """Forward (+ delta + backward) on the GPU; returns numpy float64 results and counters."""
+            dq_mode="atomic", pair_cta=False):
+    """Forward (+ delta + backward) on the GPU; returns numpy float64 results and counters.
+    ``pair_cta``: the forward with two CTAs per product (d = 128)."""
     d = to_dev(t)
     cnt = pfa.new_counters()
     o, lse = pfa.forward(d["q"], d["k"], d["v"], causal=causal, scale=scale, fix_mode=fix_mode,
-                         beta=beta, eps=eps, counters=cnt)
+                         beta=beta, eps=eps, counters=cnt, pair_cta=pair_cta)
     out = {"o": o, "lse": lse}
     if bwd:
         dq, dk, dv, delta = pfa.backward(d["q"], d["k"], d["v"], o, lse, d["do"], causal=causal,

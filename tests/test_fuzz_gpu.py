@@ -1,5 +1,6 @@
 """A randomised parity sweep with fixed seeds. Each case draws the shape (B, H_q, H_kv, N, d),
-the causal mask, the fix mode, beta, eps and the scale, the delta variant and the dQ path.
+the causal mask, the fix mode, beta, eps and the scale, the delta variant, the dQ path and, at
+d = 128, whether the forward pairs two CTAs on each product.
 Every output is then checked against the float64 oracle with the contract's tolerances.
 Integer-grid cases (modes 0 and 2, where no beta shift can underflow) also compare the
 counters bit for bit; Gaussian cases allow the few rows whose tie or round-to-one decision
@@ -38,8 +39,11 @@ def _cases(n=64, seed=2026):
         scale = 0.125 * math.sqrt(64 / d) if grid else rng.choice([1 / math.sqrt(d), 0.05, 0.2])
         delta_mode = rng.choice([0, 1])
         dq_mode = rng.choice(["atomic", "atomic", "deterministic", "split"])
+        # Half of the d = 128 cases run the forward with two CTAs per product; drawn from a
+        # generator of its own so that the cases above do not depend on it.
+        pair = d == 128 and random.Random(seed * 7919 + i).random() < 0.5
         out.append((i, B, group * h_kv, h_kv, N, d, causal, mode, beta, eps, scale, grid, delta_mode,
-                    dq_mode))
+                    dq_mode, pair))
     return out
 
 
@@ -47,17 +51,17 @@ def _cases(n=64, seed=2026):
 CASES = _cases(int(os.environ.get("PFA_FUZZ_CASES", "64")))
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "c{}-B{}Hq{}Hkv{}N{}d{}-{}-m{}-{}-{}".format(
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "c{}-B{}Hq{}Hkv{}N{}d{}-{}-m{}-{}-{}{}".format(
     c[0], c[1], c[2], c[3], c[4], c[5], "causal" if c[6] else "full", c[7], "grid" if c[11] else "gauss",
-    c[13]))
+    c[13], "-pair" if c[14] else ""))
 def test_random_case(case):
-    i, B, Hq, Hkv, N, d, causal, mode, beta, eps, scale, grid, delta_mode, dq_mode = case
+    i, B, Hq, Hkv, N, d, causal, mode, beta, eps, scale, grid, delta_mode, dq_mode, pair = case
     if grid:
         t = inputs.integer_grid(B, Hq, Hkv, N, d, causal=causal, n_planted=min(8, N), seed=100 + i)
     else:
         t = inputs.gaussian(B, Hq, Hkv, N, d, std_qkv=0.8, std_do=1.0, seed=100 + i)
     got = run_gpu(t, causal=causal, scale=scale, fix_mode=mode, beta=beta, eps=eps,
-                  delta_mode=delta_mode, dq_mode=dq_mode)
+                  delta_mode=delta_mode, dq_mode=dq_mode, pair_cta=pair)
     ref = oracle_full(t, causal=causal, scale=scale, fix_mode=mode, beta=beta, eps=eps)
     where = f"case {i}"
     # O and lse: the contract's rel-L2 and max-abs. A BF16 output of magnitude >= 4 is
