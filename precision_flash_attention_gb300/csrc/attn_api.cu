@@ -2,11 +2,9 @@
 // encoding, the device error word, and the launch sequence of each entry point.
 #include <cudaTypedefs.h>
 
-#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
-#include <vector>
 
 #include "pfa_internal.h"
 
@@ -199,34 +197,6 @@ int check_device() {
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   return check_device_locked(&dev);
-}
-
-void make_deal(long long n_items, int grid, int (*size)(long long item, const int* p), const int* p,
-               Deal* out) {
-  out->rounds = 0;
-  if (grid < 1 || n_items < 1 || n_items >= 65535) return;
-  const long long rounds = (n_items + grid - 1) / grid;
-  if (rounds * grid > kMaxDeal) return;
-  std::vector<long long> serp(grid, 0), load(grid, 0);
-  std::vector<int> order(grid);
-  for (int r = 0; r < rounds; ++r) {
-    // The serpentine deal, for comparison: left to right in even rounds, right to left
-    // in odd ones.
-    for (int c = 0; c < grid; ++c) {
-      const long long it = static_cast<long long>(r) * grid + ((r & 1) ? grid - 1 - c : c);
-      if (it < n_items) serp[c] += size(it, p);
-    }
-    for (int c = 0; c < grid; ++c) order[c] = c;
-    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return load[x] < load[y]; });
-    for (int i = 0; i < grid; ++i) {
-      const long long it = static_cast<long long>(r) * grid + i;
-      const int c = order[i];
-      out->item[r * grid + c] = static_cast<uint16_t>(it < n_items ? it : n_items);
-      if (it < n_items) load[c] += size(it, p);
-    }
-  }
-  if (*std::max_element(load.begin(), load.end()) < *std::max_element(serp.begin(), serp.end()))
-    out->rounds = static_cast<int>(rounds);
 }
 
 void note_cuda_error(cudaError_t e) {

@@ -12,10 +12,7 @@
 // from the saved lse whatever shift the forward pass used.
 //
 // Persistent: one CTA per SM takes items in heavy-first order (key tile 0 has
-// the most causal work), in rounds of gridDim.x: dealt by the host's table where
-// that leaves the busiest CTA less work (each round's items, largest first, to the
-// CTAs with the least work so far), else serpentine (left to right in even rounds,
-// right to left in odd ones). Barrier phases
+// the most causal work), dealt in serpentine rounds of gridDim.x. Barrier phases
 // count the CTA's query tiles across items, so an item's first products start
 // while the previous item's last dQ is drained and its dK / dV are stored, and
 // setup and teardown happen once per SM.
@@ -36,8 +33,6 @@
 // Tensor-core order per query tile i: dV(i), S^T(i+1), dK(i), then at d = 64
 // dP^T(i+1) and dQ(i), at d = 128 (dQ over dP^T) dQ(i) and dP^T(i+1), so the next
 // tile's scores are ready when the compute warps finish dS(i).
-#include <algorithm>
-
 #include "pfa_device.cuh"
 #include "pfa_trace.cuh"
 
@@ -115,8 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdQ, const __grid_constant__ CUtensorMap tmdK,
-                    const __grid_constant__ CUtensorMap tmdV, const BwdArgs args,
-                    const __grid_constant__ Deal deal) {
+                    const __grid_constant__ CUtensorMap tmdV, const BwdArgs args) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -167,13 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   const int item0 = static_cast<int>(blockIdx.x);
   const int stride = static_cast<int>(gridDim.x);
-  // The k-th item of this CTA: from the host's deal when it has one, else rounds
-  // of gridDim.x items, taken left to right in even rounds and right to left in odd
-  // ones, so that a CTA given a heavy item early gets a light one in the next round.
-  auto item_at = [&](int k) {
-    if (deal.rounds > 0) return k < deal.rounds ? static_cast<int>(deal.item[k * stride + item0]) : n_items;
-    return k * stride + ((k & 1) ? stride - 1 - item0 : item0);
-  };
+  // The k-th item of this CTA: rounds of gridDim.x items, taken left to right in
+  // even rounds and right to left in odd ones, so that a CTA given a heavy item
+  // early gets a light one in the next round.
+  auto item_at = [&](int k) { return k * stride + ((k & 1) ? stride - 1 - item0 : item0); };
 
   if (threadIdx.x == 0) {
     *abort_flag = (sbase & 1023u) ? 1 : 0;
@@ -229,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int g = 0;        // query tiles issued by this CTA (all items)
         bool ok = true;
-        for (int k = 0, item = item_at(0); ok && item < n_items; ++k, item = item_at(k)) {
+        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
           const Item it = decode(item);
           QCursor pc = first_of(it);
           for (int i = 0; i < it.n_iter; ++i, ++g, pc = advance(pc, it)) {
@@ -257,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc_warp(&tmV);
         int kv = 0;
         bool ok = true;
-        for (int k = 0, item = item_at(0); item < n_items; ++k, item = item_at(k)) {
+        for (int k = 0, item = item0; item < n_items; ++k, item = item_at(k)) {
           const Item it = decode(item);
           if (kv > 0 && !(ok = wait_warp(bar(L::bKVEmpty), (kv - 1) & 1, ctl))) break;
           mbar_arrive_expect_tx_warp(bar(L::bKVFull), 2 * L::kTileBytes);
@@ -279,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #if defined(PFA_TRACE) && defined(PFA_TRACE_QOBS)
       } else if (warp == 3) {
         // Trace builds only: time at which each query stage of the first item lands.
-        const Item it0 = decode(item_at(0));
+        const Item it0 = decode(item0);
         for (int g = 0; g < it0.n_iter && g < 1000; ++g) {
           if (!wait_drain(bar(L::bQFull + g % L::kStages), (g / L::kStages) & 1, ctl)) break;
           if (lane == 0) PFA_BWD_TRACE(6, 42, g);
@@ -321,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0;
         int kv = 0;
         bool ok = true;
-        for (int k = 0, item = item_at(0); ok && item < n_items; ++k, item = item_at(k), ++kv) {
+        for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
           const Item it = decode(item);
           if (!(ok = wait_warp(bar(L::bKVFull), kv & 1, ctl))) break;
           if (lane == 0) PFA_BWD_TRACE(0, 37, kv);
@@ -430,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0;
       int kv = 0;   // items drained (the MMADone phases)
-      for (int k = 0, item = item_at(0); ok && item < n_items; ++k, item = item_at(k)) {
+      for (int k = 0, item = item0; ok && item < n_items; ++k, item = item_at(k)) {
         const Item itm = decode(item);
         QCursor qc = first_of(itm);
         for (int i = 0; DQ && ok && i < itm.n_iter; ++i, ++g, qc = advance(qc, itm)) {
@@ -570,14 +561,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       float pre = 0.f;
       bool pre_in = false;
-      if (item_at(0) < n_items) {
-        const float* src = stage_src(first_of(decode(item_at(0))));
+      if (item0 < n_items) {
+        const float* src = stage_src(first_of(decode(item0)));
         pre_in = src != nullptr;
         if (pre_in) pre = ld_global_early(src);
       }
 
       int g = 0;   // query tiles of this CTA so far (all items): the barrier phases
-      for (int k = 0, item = item_at(0), kv = 0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
+      for (int k = 0, item = item0, kv = 0; ok && item < n_items; ++k, item = item_at(k), ++kv) {
       const Item itm = decode(item);
       const int k0 = itm.k0;
       const int key = k0 + r;
@@ -758,27 +749,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long n_items = static_cast<long long>((a.s.N + kTile - 1) / kTile) * a.s.B * a.s.Hkv;
   const dim3 grid(static_cast<unsigned>(n_items < sms ? n_items : sms));
-  // One deal per thread for the shape last launched from it.
-  struct Cached {
-    int key[5] = {-1, -1, -1, -1, -1};
-    Deal deal;
-  };
-  thread_local Cached cache;
-  const int n_t = (a.s.N + kTile - 1) / kTile, bh_kv = a.s.B * a.s.Hkv, group = a.s.Hq / a.s.Hkv;
-  const int key[5] = {n_t, bh_kv, group, CAUSAL ? 1 : 0, static_cast<int>(grid.x)};
-  if (!std::equal(key, key + 5, cache.key)) {
-    // Query tiles an item visits: from its key tile kt = item / bh_kv on (all of them
-    // without the causal mask), for each of the group's query heads. Equal items
-    // (no mask) are dealt evenly by the serpentine rounds.
-    cache.deal.rounds = 0;
-    if (CAUSAL)
-      make_deal(n_items, static_cast<int>(grid.x),
-                [](long long item, const int* p) { return p[2] * (p[0] - static_cast<int>(item / p[1])); },
-                key, &cache.deal);
-    std::copy(key, key + 5, cache.key);
-  }
-  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, tdo, tdq, tdk, tdv, a,
-                    cache.deal);
+  return launch_pdl(kern, grid, dim3(kThreads), L::kBytes, stream, tq, tk, tv, tdo, tdq, tdk, tdv, a);
 }
 
 __global__ void zero_kernel(float4* __restrict__ dst, long long n4) {

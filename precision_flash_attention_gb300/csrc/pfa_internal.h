@@ -84,22 +84,6 @@ struct BwdArgs {
   unsigned long long* err_site;
 };
 
-// A static deal of a persistent kernel's work items (in order, heaviest first)
-// over its CTAs: item[r * grid + c] is CTA c's item in round r (n_items where it
-// has none). rounds == 0: the kernel deals serpentine rounds itself.
-constexpr int kMaxDeal = 152 * 8;
-struct Deal {
-  int rounds;
-  uint16_t item[kMaxDeal];
-};
-
-// Rounds of `grid` items in order; each round's items, largest first, go to the CTAs
-// with the least work so far (ties by index). `size(i)` is item i's work. Kept only
-// where its busiest CTA has less work than under the serpentine deal and the table
-// fits (n_items < 65535, rounds x grid <= kMaxDeal); otherwise out->rounds = 0.
-void make_deal(long long n_items, int grid, int (*size)(long long item, const int* p), const int* p,
-               Deal* out);
-
 struct DqArgs {
   AttnShape s;
   const float* lse;

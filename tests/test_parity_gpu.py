@@ -269,18 +269,16 @@ def test_gpt2_small_layer_all_heads():
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_backward_dealt_from_a_table(d):
+def test_three_rounds_of_key_tiles(d):
     # B = 4, H = 12, N = 1024, causal: 384 key-tile items (1 to 8 query tiles each) over 152
-    # CTAs, where the host's deal (each round's items to the CTAs with the least work so
-    # far) leaves the busiest CTA 12 query tiles against 13 under the serpentine deal and
-    # replaces it. Every head against the oracle; at d = 128 the kernel without its dQ
-    # product (the query-outer pass computes dQ).
+    # CTAs, three serpentine rounds with a partial last one. Every head against the oracle;
+    # at d = 128 the kernel without its dQ product (the query-outer pass computes dQ).
     t = inputs.gaussian(4, 12, 12, 1024, d, std_qkv=0.7, std_do=1.0, seed=d)
     kw = dict(causal=True, scale=d ** -0.5, fix_mode=1, beta=2.0)
     got = run_gpu(t, **kw)
     ref = oracle_full(t, **kw)
-    assert_fwd_close(got, ref, f"dealt d={d}")
-    assert_bwd_close(got, ref, f"dealt d={d}")
+    assert_fwd_close(got, ref, f"B4 H12 N1024 d={d}")
+    assert_bwd_close(got, ref, f"B4 H12 N1024 d={d}")
 
 
 def test_gpt2_shape_n2048_sampled_rows():
