@@ -135,3 +135,38 @@ def test_pair_flag_is_refused_where_not_built():
         pfa.attn_fwd_ex(t["q"], t["k"], t["v"], o, lse, causal=False, scale=0.1, monitor=pfa.new_monitor(),
                         flags=pfa.FWD_PAIR_CTA)
     assert pfa.device_error() == 0
+
+
+def test_pair_forward_in_a_cuda_graph():
+    # The paired forward is a cluster launch chained by programmatic dependent launch; it
+    # captures into a CUDA graph with a backward call after it, and the replay gives the
+    # eager results (dQ by the deterministic pass, so bit for bit).
+    t = to_dev(inputs.gaussian(1, 4, 2, 700, 128, std_qkv=0.7, std_do=1.0, seed=13))
+    q, k, v, do = t["q"], t["k"], t["v"], t["do"]
+    o, lse = torch.empty_like(q), torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    kw = dict(causal=True, scale=128 ** -0.5)
+
+    def step():
+        pfa.attn_fwd_ex(q, k, v, o, lse, fix_mode=1, beta=2.0, eps=1e-3, flags=pfa.FWD_PAIR_CTA, **kw)
+        pfa.attn_delta(o, do, delta)
+        pfa.attn_bwd_ex(q, k, v, do, lse, delta, dq, dk, dv, None, flags=pfa.BWD_DQ_DETERMINISTIC, **kw)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (o, lse, dq, dk, dv)]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for x in (o, lse, dq, dk, dv):
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert pfa.device_error(clear=True) == 0
+    for a, b in zip(eager, (o, lse, dq, dk, dv)):
+        assert torch.equal(a, b)
