@@ -239,7 +239,7 @@ int pfa_attn_bwd_accum(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, 
  * without its zeroing pass. With PFA_BWD_DQ_DETERMINISTIC or
  * PFA_BWD_DQ_SPLIT the key-outer kernel computes dK and dV only, and a
  * query-outer pass recomputes S, P, dP and dS per query tile to form
- * dQ = alpha dS K (the equation of pfa_attn_bwd, [PK] equations): it costs two
+ * dQ = dS K (the equation of pfa_attn_bwd, [PK] equations; alpha is in dS): it costs two
  * more products per tile pair (S and dP again) and, with the split, a second dQ
  * product. dq_accum is then not used and may be NULL. Other unknown flag bits
  * return PFA_ERR_INVALID_ARG. Same arguments, layouts and checks as

@@ -340,7 +340,7 @@ struct BwdLaunch {
 };
 
 // The argument checks shared by pfa_attn_bwd and pfa_attn_bwd_accum, and the
-// tensor maps and arguments of the kernel (dq_accum += alpha dS K; dk, dv written).
+// tensor maps and arguments of the kernel (dq_accum += alpha (P o (dP - delta)) K; dk, dv written).
 // dq_accum may be null only when the query-outer pass computes dQ (need_accum false).
 int bwd_check(const pfa_bf16* q, const pfa_bf16* k, const pfa_bf16* v, const pfa_bf16* dO,
               const float* lse, const float* delta, const float* dq_accum, const pfa_bf16* dk,
@@ -395,7 +395,7 @@ int bwd_launch(const BwdLaunch& L, cudaStream_t st) {
 }
 
 // dK, dV from the key-outer kernel without its dQ product (L prepared with no dQ
-// workspace), then dQ = alpha dS K from the query-outer pass (split: dS as BF16 hi + lo).
+// workspace), then dQ = alpha (P o (dP - delta)) K from the query-outer pass (split: dS as BF16 hi + lo).
 int bwd_query_outer(const BwdLaunch& L, pfa_bf16* dq, const float* lse, const float* delta, bool split,
                     cudaStream_t st) {
   pfa::DqArgs da;

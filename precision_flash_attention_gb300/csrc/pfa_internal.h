@@ -120,7 +120,7 @@ cudaError_t launch_delta_alt(const CUtensorMap& tq, const CUtensorMap& tk, const
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdq, const CUtensorMap& tdk,
                        const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t stream);
-// dQ = alpha dS K by the query-outer pass (deterministic; hi/lo dS when a.split).
+// dQ = alpha (P o (dP - delta)) K by the query-outer pass (deterministic; hi/lo dS when a.split).
 cudaError_t launch_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const DqArgs& a, cudaStream_t stream);
 cudaError_t launch_convert_dq(const float* dq_accum, void* dq, long long n, cudaStream_t stream);
