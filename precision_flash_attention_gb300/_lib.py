@@ -24,6 +24,9 @@ FWD_PBAR_MXFP4 = 4
 FWD_PAIR_CTA = 8
 TIE_BINS = 8
 MONITOR_WORDS = 1 + TIE_BINS
+# bits of the device error word (pfa_device_error)
+DEVERR_TIMEOUT = 1
+DEVERR_SMEM_ALIGN = 2
 # pfa_attn_bwd_ex flags (include/pfa.h)
 BWD_DQ_DETERMINISTIC = 1
 BWD_DQ_SPLIT = 2

@@ -33,7 +33,8 @@ def test_binding_constants_match_the_header():
     text = re.sub(r"/\*.*?\*/", "", open(HEADER, encoding="utf-8").read(), flags=re.S)
     defines = {n: int(v) for n, v in re.findall(r"#define\s+PFA_([A-Z0-9_]+)\s+(\d+)u?\b", text)}
     for name in ("FWD_UNFUSED_BF16_PV", "FWD_PBAR_E4M3", "FWD_PBAR_MXFP4", "FWD_PAIR_CTA",
-                 "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "BWD_WORKSPACE_ZEROED", "TIE_BINS"):
+                 "BWD_DQ_DETERMINISTIC", "BWD_DQ_SPLIT", "BWD_WORKSPACE_ZEROED", "TIE_BINS",
+                 "DEVERR_TIMEOUT", "DEVERR_SMEM_ALIGN"):
         assert getattr(_lib, name) == defines[name], name
     status = {int(v): "PFA_" + n for n, v in re.findall(r"\bPFA_((?:OK|ERR_[A-Z_]+))\s*=\s*(-?\d+)", text)}
     assert status == _lib.STATUS_NAMES

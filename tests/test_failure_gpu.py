@@ -9,13 +9,13 @@ import pytest
 import torch
 
 import precision_flash_attention_gb300 as pfa
-from precision_flash_attention_gb300 import inputs
+from precision_flash_attention_gb300 import _lib, inputs
 
 from gpu_helpers import assert_bwd_close, assert_fwd_close, oracle_full, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-PFA_DEVERR_TIMEOUT = 1
+PFA_DEVERR_TIMEOUT = _lib.DEVERR_TIMEOUT   # checked against include/pfa.h by the ABI tests
 
 
 @pytest.fixture(scope="module", autouse=True)
