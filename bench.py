@@ -803,7 +803,7 @@ def run_gpu_arm(args):
     sweep = {}
     _progress(args, f"timed steps done: {ms:.3f} ms per step")
     if args.sweep and rank == 0:
-        for n_s in (2048, 4096, 8192):
+        for n_s in (2048, 4096, 8192, 16384):
             ts = make_inputs(dev, B, H, n_s, d, seed=1)
             k_s = max(3, args.steps // 2)
             sts = {m: Step(ts, causal=True, scale=w["scale"], fix_mode=m, beta=w["beta"], eps=w["eps"])
